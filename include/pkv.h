@@ -1,0 +1,178 @@
+/*
+ * pkv.h -- C ABI of libpkv: decode-step paged attention over a
+ * block-table-indexed KV cache, fp16 or INT8 KV, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources for what each call computes:
+ *  [PKF]  "PagedKV-Fusion" README (INT8 per-(block, head) quantized decode
+ *         attention): "Overview" component B, "Architecture" flowchart
+ *         ("per-block,head symmetric INT8", "online softmax . GQA") and
+ *         sequence diagram ("INT8 survivors + scales", "decode step (block
+ *         table)"), "Memory footprint" table.
+ *  [PAR]  "paged-attention-runtime" summary: CORE CAPABILITIES 1 (16-token
+ *         blocks) and 2 (block-table indirection, online softmax, FP32
+ *         accumulation), 4 (GQA).
+ *  [GLO]  "PagedAttention & KV-Cache Memory Management": section 2.1 (block
+ *         table: block = table[t / B], slot = t % B).
+ *
+ * Layouts (all row-major, all pointers are DEVICE pointers owned by the
+ * caller; the library never allocates, frees or synchronises):
+ *   K/V pools      [num_blocks][num_kv_heads][block_size][head_dim]
+ *                  (one contiguous tile per (block, kv head))
+ *   scales         [num_blocks][num_kv_heads]  fp32, one for K, one for V
+ *   query          [num_seqs][num_heads][head_dim]  fp16
+ *   block_tables   [num_seqs][max_blocks_per_seq]   int32 physical ids
+ *   context_lens   [num_seqs]                        int32
+ *   out            [num_seqs][num_heads][head_dim]  fp32
+ * Query head h attends with kv head h / (num_heads / num_kv_heads).
+ * Supported: block_size 16; head_dim 64 or 128; any group size.
+ *
+ * Errors.  Host-side argument errors are returned before anything is
+ * launched.  Device-side data errors never trap: the affected outputs are
+ * written as zeros and a bit is OR-ed into the optional caller-owned int32
+ * *dev_status (device memory; the caller zeroes it).  Every wait inside a
+ * kernel is bounded (about one second); a wait that runs out sets
+ * PKV_DEV_TIMEOUT and the kernel returns.  Calls are asynchronous on the
+ * given stream (NULL = the legacy default stream); a launch failure is
+ * reported as PKV_ERR_CUDA.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1, /* null pointer, negative size, heads not divisible, ... */
+    PKV_ERR_UNSUPPORTED = 2, /* block_size != 16, head_dim not 64/128, size limits */
+    PKV_ERR_MISALIGNED = 3,  /* a pointer misses its required alignment */
+    PKV_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+    PKV_ERR_CUDA = 5         /* a CUDA runtime call or launch failed */
+} pkv_status;
+
+/* Bits of *dev_status. */
+#define PKV_DEV_BAD_BLOCK 1u /* a block id outside [0, num_blocks) was needed */
+#define PKV_DEV_BAD_CTX 2u   /* context_lens[s] outside [0, max_context_len] or
+                                beyond max_blocks_per_seq * block_size */
+#define PKV_DEV_TIMEOUT 4u   /* a bounded wait for an asynchronous copy ran out */
+
+/*
+ * pkv_quantize_blocks -- symmetric per-(block, kv head) INT8 quantization
+ * of fp16 K and V tiles ([PKF] Overview component B; sequence diagram
+ * "INT8 survivors + scales").
+ *
+ * For every listed block b and kv head h, separately for K and V, over all
+ * block_size * head_dim values x of the tile (padding slots included):
+ *   amax  = max |x| in fp32 (NaN values ignored)
+ *   scale = amax / 127            (IEEE fp32 division)
+ *   code  = round-half-to-even(x / scale) clamped to [-127, 127]
+ *           (x / scale rounded to fp32 first; a NaN quotient -- 0/0, inf/inf,
+ *           NaN input -- gives code 0)
+ * Codes go to the same (b, h) tile of k_codes / v_codes, scales to
+ * k_scales[b][h] / v_scales[b][h].  Results are bit-identical to the CPU
+ * oracle of this repository.
+ *
+ *   k_fp16, v_fp16     const fp16 pools, 16-byte aligned
+ *   k_codes, v_codes   int8 pools of the same shape, 16-byte aligned
+ *   k_scales, v_scales fp32 [num_blocks][num_kv_heads], 4-byte aligned
+ *   block_ids          device int32 [num_ids] or NULL for all blocks;
+ *                      duplicates allowed (same result); ids outside
+ *                      [0, num_blocks) are skipped and set PKV_DEV_BAD_BLOCK
+ *   dev_status         optional device int32 (may be NULL)
+ *   stream             cudaStream_t as void*
+ */
+pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16,
+                               int8_t *k_codes, int8_t *v_codes,
+                               float *k_scales, float *v_scales,
+                               const int32_t *block_ids, int num_ids,
+                               int num_blocks, int num_kv_heads, int head_dim,
+                               int block_size, int32_t *dev_status,
+                               void *stream);
+
+/*
+ * pkv_paged_decode_fp16 -- one decode step of paged attention over fp16 KV
+ * ([PKF] sequence diagram "decode step (block table)"; [PAR] CORE
+ * CAPABILITIES 2 and 4; [GLO] section 2.1).
+ *
+ * For every sequence s (ctx = context_lens[s]) and query head h with kv head
+ * kvh = h / (num_heads / num_kv_heads):
+ *   K_t = k_cache[block_tables[s][t / 16]][kvh][t % 16][:]   (t < ctx)
+ *   z_t = softmax_scale * <query[s][h], K_t>
+ *   out[s][h] = sum_t softmax(z)_t * V_t      (FP32 accumulation)
+ * ctx == 0 gives zeros.  Slots t >= ctx of the last block are never used
+ * (they may hold anything, NaN included).  Table entries past the context
+ * are never read.
+ *
+ *   out            fp32 [num_seqs][num_heads][head_dim], 16-byte aligned
+ *   query          fp16, 16-byte aligned
+ *   k_cache/v_cache fp16 pools, 16-byte aligned, num_blocks blocks
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens   int32 [num_seqs]
+ *   max_context_len host bound on every context_lens[s] (sizes the launch;
+ *                  a larger length on the device is PKV_DEV_BAD_CTX)
+ *   workspace      device scratch of at least pkv_decode_workspace_size()
+ *                  bytes, 16-byte aligned; contents need no initialisation
+ *                  and are overwritten
+ *   dev_status     optional device int32 (may be NULL)
+ * Two calls sharing a workspace must not overlap on the GPU.
+ * num_seqs == 0 returns PKV_OK without launching.
+ */
+pkv_status pkv_paged_decode_fp16(float *out, const void *query,
+                                 const void *k_cache, const void *v_cache,
+                                 int num_blocks, const int32_t *block_tables,
+                                 int max_blocks_per_seq,
+                                 const int32_t *context_lens,
+                                 int max_context_len, int num_seqs,
+                                 int num_heads, int num_kv_heads, int head_dim,
+                                 int block_size, float softmax_scale,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream);
+
+/*
+ * pkv_paged_decode_int8 -- the same decode step over INT8 KV with one fp32
+ * scale per (block, kv head) for K and one for V ([PKF] Overview component
+ * B, "Architecture" flowchart): K_t = k_codes[...] * k_scales[blk][kvh],
+ * V_t = v_codes[...] * v_scales[blk][kvh], as produced by
+ * pkv_quantize_blocks.  Arguments as for pkv_paged_decode_fp16, with
+ *   k_codes/v_codes  int8 pools, 16-byte aligned
+ *   k_scales/v_scales fp32 [num_blocks][num_kv_heads], 4-byte aligned
+ */
+pkv_status pkv_paged_decode_int8(float *out, const void *query,
+                                 const int8_t *k_codes, const int8_t *v_codes,
+                                 const float *k_scales, const float *v_scales,
+                                 int num_blocks, const int32_t *block_tables,
+                                 int max_blocks_per_seq,
+                                 const int32_t *context_lens,
+                                 int max_context_len, int num_seqs,
+                                 int num_heads, int num_kv_heads, int head_dim,
+                                 int block_size, float softmax_scale,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream);
+
+/*
+ * Bytes of workspace a decode call with these sizes needs (either variant).
+ * Pure host arithmetic: no CUDA call.  Returns 0 for invalid sizes.
+ */
+size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int max_context_len);
+
+/*
+ * Tuning and test control: cap the number of decode workers (one worker =
+ * one warp streaming a contiguous range of KV pages; each range ends in a
+ * partial result that the split-context reduce merges).  0 restores the
+ * automatic choice (every resident warp of the device).  Process-wide.
+ */
+pkv_status pkv_set_decode_workers(int max_workers);
+
+/* Static description of a status code. */
+const char *pkv_status_string(pkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,252 @@
+/*
+ * pkv_oracle.c -- plain CPU oracle for paged decode attention and for the
+ * per-(block, kv-head) symmetric INT8 quantizer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the package smoke check and the timed CPU
+ * baseline of the benchmark use it.  It shares no source, header, table or
+ * helper with the CUDA library; the two only ever see the same seeded inputs.
+ *
+ * What it computes, and where that is defined:
+ *
+ *  - pkv_oracle_decode: single-query attention for every (sequence, query
+ *    head), gathering K and V token by token through the block table, then a
+ *    dense max-subtracted softmax and a weighted sum of V, all in fp64.
+ *      * block-table address translation: physical block = table[t / B],
+ *        slot = t % B ("PagedAttention & KV-Cache Memory Management",
+ *        section 2.1 "Logical Token Blocks & Page Tables");
+ *      * softmax attention with FP32-or-better accumulation, GQA head groups
+ *        ("paged-attention-runtime" summary, "CORE CAPABILITIES" 2 and 4;
+ *        PagedKV-Fusion README, "Architecture", component B "online softmax
+ *        . GQA").  The online (streaming) softmax of the kernels is an exact
+ *        reformulation of this dense softmax, so the oracle uses the dense
+ *        form, which is the plain definition.
+ *      * INT8 KV: value = code * scale with one fp32 scale per (block,
+ *        kv-head) for K and one for V (PagedKV-Fusion README, "Overview",
+ *        component B, and the "Memory footprint" table whose exact MiB
+ *        figures fix that granularity).
+ *
+ *  - pkv_oracle_quantize: per (block, kv-head) tile of B x d fp16 values,
+ *    amax = max |x| in fp32, scale = amax / 127 (fp32 division),
+ *    code = round-half-to-even(x / scale) clamped to [-127, 127]
+ *    (PagedKV-Fusion README, "Overview" component B and "Architecture":
+ *    "per-block,head symmetric INT8").  The pages say "symmetric" only; the
+ *    absmax/127 scale, the rounding mode and the NaN rules are the readings
+ *    this project adopts (they are listed with the other readings in the
+ *    design notes).  Computed in fp32 so that codes and scales can be
+ *    compared bit for bit.
+ *
+ * Conventions shared with the library (by specification, not by code):
+ *   pools    [num_blocks][num_kv_heads][block_size][head_dim]
+ *   scales   [num_blocks][num_kv_heads]
+ *   query    [num_seqs][num_heads][head_dim]        (fp16 bit patterns)
+ *   tables   [num_seqs][max_blocks_per_seq]         (int32)
+ *   out      [num_seqs][num_heads][head_dim]        (fp64 here)
+ *   q head h reads kv head h / (num_heads / num_kv_heads).
+ * Per-(seq, head) flags: bit 0 = a block id outside [0, num_blocks) was
+ * needed, bit 1 = the context length is outside [0, min(max_context_len,
+ * max_blocks_per_seq * block_size)].  A flagged (seq, head) outputs zeros;
+ * context length 0 outputs zeros with no flag.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_BAD_BLOCK 1u
+#define ORACLE_BAD_CTX 2u
+
+/* IEEE binary16 bit pattern -> exact double (every half is a double). */
+double pkv_oracle_half_to_double(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 10) & 0x1f;
+    const int mant = h & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)mant, -24); /* subnormal: mant * 2^-24 */
+    } else if (expo == 31) {
+        v = mant ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(mant | 0x400), expo - 25); /* 1.mant * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* One element of K or V for token slot `slot` of physical block `blk`. */
+static double kv_element(int kv_kind, const void *pool, const float *scales,
+                         int64_t blk, int kvh, int slot, int i,
+                         int num_kv_heads, int block_size, int head_dim)
+{
+    const int64_t tile = blk * num_kv_heads + kvh;
+    const int64_t idx = (tile * block_size + slot) * head_dim + i;
+    if (kv_kind == 0) {
+        return pkv_oracle_half_to_double(((const uint16_t *)pool)[idx]);
+    }
+    return (double)((const int8_t *)pool)[idx] * (double)scales[tile];
+}
+
+/*
+ * kv_kind 0: kpool/vpool are fp16 bit patterns, kscale/vscale ignored.
+ * kv_kind 1: kpool/vpool are int8 codes, kscale/vscale fp32 per tile.
+ * flags: optional [num_seqs][num_heads] output (may be NULL).
+ * Returns 0, or -1 on an argument the oracle cannot interpret.
+ */
+int pkv_oracle_decode(double *out, const uint16_t *query, int kv_kind,
+                      const void *kpool, const void *vpool,
+                      const float *kscale, const float *vscale,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      int num_seqs, int num_heads, int num_kv_heads,
+                      int head_dim, int block_size, int max_blocks_per_seq,
+                      int64_t num_blocks, int max_context_len,
+                      double softmax_scale, int num_threads, uint32_t *flags)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
+        max_blocks_per_seq < 0 || (kv_kind != 0 && kv_kind != 1)) {
+        return -1;
+    }
+    const int group = num_heads / num_kv_heads;
+    const int64_t pairs = (int64_t)num_seqs * num_heads;
+    int64_t ctx_cap = (int64_t)max_blocks_per_seq * block_size;
+    if (max_context_len < ctx_cap) ctx_cap = max_context_len;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+
+#pragma omp parallel
+    {
+        int cap = 0;
+        double *z = NULL; /* scores of one (seq, head) */
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t pair = 0; pair < pairs; ++pair) {
+            const int s = (int)(pair / num_heads);
+            const int h = (int)(pair % num_heads);
+            const int kvh = h / group;
+            double *o = out + pair * head_dim;
+            const uint16_t *qv = query + pair * head_dim;
+            const int ctx = context_lens[s];
+            uint32_t flag = 0;
+            for (int i = 0; i < head_dim; ++i) o[i] = 0.0;
+
+            if (ctx < 0 || ctx > ctx_cap) flag |= ORACLE_BAD_CTX;
+            /* every block the context needs must be a real block */
+            for (int t = 0; !flag && t < ctx; t += block_size) {
+                const int32_t blk = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+                if (blk < 0 || blk >= num_blocks) flag |= ORACLE_BAD_BLOCK;
+            }
+            if (flags) flags[pair] = flag;
+            if (flag || ctx == 0) continue;
+
+            if (ctx > cap) {
+                free(z);
+                cap = ctx;
+                z = (double *)malloc(sizeof(double) * (size_t)cap);
+            }
+            /* scores z_t = softmax_scale * <q, K_t> over the gathered keys */
+            for (int t = 0; t < ctx; ++t) {
+                const int64_t blk = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+                const int slot = t % block_size;
+                double dot = 0.0;
+                for (int i = 0; i < head_dim; ++i) {
+                    const double qi = pkv_oracle_half_to_double(qv[i]);
+                    const double ki = kv_element(kv_kind, kpool, kscale, blk, kvh, slot, i,
+                                                 num_kv_heads, block_size, head_dim);
+                    dot += qi * ki;
+                }
+                z[t] = softmax_scale * dot;
+            }
+            /* softmax weights w_t = exp(z_t - max z) / sum exp(z - max z) */
+            double zmax = z[0];
+            for (int t = 1; t < ctx; ++t) if (z[t] > zmax) zmax = z[t];
+            double denom = 0.0;
+            for (int t = 0; t < ctx; ++t) {
+                z[t] = exp(z[t] - zmax);
+                denom += z[t];
+            }
+            /* out = sum_t w_t V_t */
+            for (int t = 0; t < ctx; ++t) {
+                const int64_t blk = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+                const int slot = t % block_size;
+                const double w = z[t] / denom;
+                for (int i = 0; i < head_dim; ++i) {
+                    o[i] += w * kv_element(kv_kind, vpool, vscale, blk, kvh, slot, i,
+                                           num_kv_heads, block_size, head_dim);
+                }
+            }
+        }
+        free(z);
+    }
+    return 0;
+}
+
+/* Quantize one tile of n fp16 values (bit patterns) into codes + scale. */
+static void quantize_tile(int8_t *codes, float *scale_out, const uint16_t *x, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t e = 0; e < n; ++e) {
+        const float a = fabsf((float)pkv_oracle_half_to_double(x[e]));
+        if (a > amax) amax = a; /* NaN never compares greater: ignored */
+    }
+    const float scale = amax / 127.0f;
+    for (int64_t e = 0; e < n; ++e) {
+        const float v = (float)pkv_oracle_half_to_double(x[e]);
+        const float y = v / scale; /* 0/0 and inf/inf give NaN -> code 0 */
+        int c = 0;
+        if (!isnan(y)) {
+            float r = nearbyintf(y); /* default rounding: to nearest, ties to even */
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            c = (int)r;
+        }
+        codes[e] = (int8_t)c;
+    }
+    *scale_out = scale;
+}
+
+/*
+ * Quantize the tiles (block_ids[j], kv-head) of one fp16 pool.
+ * block_ids == NULL means every block 0..num_blocks-1 in order.
+ * Codes and scales are written at the same (block, kv-head) positions of
+ * code_pool [num_blocks][num_kv_heads][block_size][head_dim] and
+ * scales [num_blocks][num_kv_heads].  Returns the number of ids outside
+ * [0, num_blocks) (those are skipped), or -1 on bad arguments.
+ */
+int64_t pkv_oracle_quantize(int8_t *code_pool, float *scales, const uint16_t *pool,
+                            const int32_t *block_ids, int64_t num_ids,
+                            int64_t num_blocks, int num_kv_heads, int block_size,
+                            int head_dim)
+{
+    if (num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 || head_dim <= 0) return -1;
+    const int64_t tile_elems = (int64_t)block_size * head_dim;
+    const int64_t count = block_ids ? num_ids : num_blocks;
+    int64_t bad = 0;
+    for (int64_t j = 0; j < count; ++j) {
+        const int64_t blk = block_ids ? block_ids[j] : j;
+        if (blk < 0 || blk >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        for (int kvh = 0; kvh < num_kv_heads; ++kvh) {
+            const int64_t tile = blk * num_kv_heads + kvh;
+            quantize_tile(code_pool + tile * tile_elems, scales + tile,
+                          pool + tile * tile_elems, tile_elems);
+        }
+    }
+    return bad;
+}
+
+/* Threads the OpenMP runtime will use for a parallel region (1 without OpenMP). */
+int pkv_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
