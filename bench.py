@@ -1,0 +1,407 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one decode step of a 64-sequence batch with an INT8 KV cache:
+  1. pkv_quantize_blocks on the batch's tail blocks (the blocks that hold each
+     sequence's newest tokens, K and V),
+  2. pkv_paged_decode_int8 over the whole batch (block-table gather, INT8
+     dequant, QK^T, online softmax, PV, split-context reduce, GQA).
+Workload: 64 seqs x ctx 2048, 32 q / 8 kv heads, head_dim 128, block 16, a
+65536-block pool with seeded random placement (synthetic N(0,1) data).
+
+Metric: KV GB/s = algorithmic bytes per step / step time (the bytes of K, V
+and scales a step must read plus what the quantizer reads and writes), also
+sequence-steps/s and p50 us/step.  The fp16-KV decode of the same batch is
+timed alongside and reported under "variants".
+
+--impl reference times the CPU oracle (plain C, fp64 attention) on a bounded
+sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import pkv_workloads as W  # noqa: E402
+
+CONFIG = "c5a_64x2048"
+METRIC = "paged decode attn: KV GB/s (% of HBM peak), seq-steps/s, p50 µs/step"
+UNIT = "GB/s"
+FLUSH_BYTES = 256 << 20  # > 129 MB L2: written between timed steps
+# DRAM bytes per launch of the INT8 decode (decode + reduce kernels) on this
+# workload from the ncu capture summarised in profiles/, with the hash of the
+# kernel source it was taken on; the figure is dropped when the source changes.
+TRAFFIC = {"decode_int8": None}
+
+
+def _src_hash():
+    p = os.path.join(ROOT, "paged_kv_cache_234_gb300", "csrc", "pkv_decode.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def decode_bytes(ctx, num_kv_heads, head_dim, elem_bytes, with_scales):
+    """Algorithmic bytes one decode call must read: K and V of every cached
+    token of every kv head, plus one K and one V scale per (block, kv head)."""
+    ctx = np.asarray(ctx, dtype=np.int64)
+    b = int(ctx.sum()) * num_kv_heads * head_dim * 2 * elem_bytes
+    if with_scales:
+        b += int(((ctx + 15) // 16).sum()) * num_kv_heads * 2 * 4
+    return b
+
+
+def quantize_bytes(num_tiles, head_dim):
+    """fp16 read + int8 written per value, one fp32 scale per tile (K and V)."""
+    return num_tiles * 2 * (16 * head_dim * 3 + 4)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _subpool(w, seqs):
+    """The sampled sequences' blocks gathered into a compact pool, with their
+    tables renumbered (attention does not depend on physical placement)."""
+    tab = w.block_tables[seqs]
+    lens = w.context_lens[seqs]
+    ids = np.unique(tab[tab >= 0]).astype(np.int32)
+    local = np.full(w.num_blocks, -1, np.int32)
+    local[ids] = np.arange(ids.size, dtype=np.int32)
+    ltab = np.where(tab >= 0, local[np.maximum(tab, 0)], -1).astype(np.int32)
+    tails = np.array([ltab[i, (c - 1) // 16] for i, c in enumerate(lens) if c > 0], np.int32)
+    return (np.ascontiguousarray(w.k_pool[ids]), np.ascontiguousarray(w.v_pool[ids]), ltab,
+            lens, tails)
+
+
+def run_reference(args, ws, rank):
+    """CPU oracle on a bounded sample of the workload (rank 0 only): each step
+    quantizes the tail blocks of 8 of the 64 sequences and decodes those 8."""
+    if rank != 0:
+        return
+    import oracle
+    w = W.make(CONFIG)
+    sample = 8
+    seqs = np.arange(0, w.num_seqs, w.num_seqs // sample)[:sample]
+    kp, vp, tab, lens, tails = _subpool(w, seqs)
+    kc, ks = oracle.quantize(kp)   # the cache contents, not timed
+    vc, vs = oracle.quantize(vp)
+    threads = oracle.max_threads()
+    step_b = (decode_bytes(lens, w.num_kv_heads, w.head_dim, 1, True)
+              + quantize_bytes(len(tails) * w.num_kv_heads, w.head_dim))
+    t_total = 0.0
+    for it in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.quantize(kp, block_ids=tails, code_pool=kc, scales=ks, inplace=True)
+        oracle.quantize(vp, block_ids=tails, code_pool=vc, scales=vs, inplace=True)
+        oracle.decode_int8(w.query[seqs], kc, vc, ks, vs, tab, lens,
+                           num_kv_heads=w.num_kv_heads, softmax_scale=w.softmax_scale,
+                           num_threads=threads)
+        if it >= args.warmup:
+            t_total += time.perf_counter() - t0
+    value = step_b * args.steps / t_total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_total / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{CONFIG} (CPU oracle on {sample} of {w.num_seqs} sequences "
+                               "per step)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{sample} of {w.num_seqs} sequences per step: INT8 "
+                                   "quantize of their tail blocks + fp64 INT8 decode"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, seconds=10.0):
+    """Oracle INT8 decode on a bounded sample, timed on this host's cores."""
+    import oracle
+    threads = oracle.max_threads()
+    seqs = np.arange(4)
+    kp, vp, tab, lens, _ = _subpool(w, seqs)
+    kc, ks = oracle.quantize(kp)
+    vc, vs = oracle.quantize(vp)
+    nb = decode_bytes(lens, w.num_kv_heads, w.head_dim, 1, True)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.decode_int8(w.query[seqs], kc, vc, ks, vs, tab, lens,
+                           num_kv_heads=w.num_kv_heads, softmax_scale=w.softmax_scale,
+                           num_threads=threads)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"value": nb * reps / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"fp64 INT8 decode of 4 of {w.num_seqs} sequences, repeated {reps} times "
+                      f"({dt:.1f} s)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    import paged_kv_cache_234_gb300 as pkv
+    from paged_kv_cache_234_gb300 import build as pkv_build
+
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    if rank == 0:
+        pkv_build.build()
+    if pg:
+        pg.barrier()
+    pkv.lib()
+
+    w = W.make(CONFIG)
+    n, hq, d = w.query.shape
+    hkv = w.num_kv_heads
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    kf, vf = dev(w.k_pool), dev(w.v_pool)
+    q, bt, cl = dev(w.query), dev(w.block_tables), dev(w.context_lens)
+    kc = torch.zeros(w.k_pool.shape, dtype=torch.int8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros(w.k_pool.shape[:2], dtype=torch.float32, device="cuda")
+    vs = torch.zeros_like(ks)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    used = dev(w.used_block_ids)
+    tails_np = w.tail_block_ids()
+    tails = dev(tails_np)
+    mcl = w.max_context_len
+    ws_t = pkv.decode_workspace(n, hq, hkv, d, mcl)
+    out = torch.empty((n, hq, d), dtype=torch.float32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # the cache contents: every used block quantized once (not timed)
+    pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, used, status)
+    torch.cuda.synchronize()
+
+    def step_int8():
+        pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, tails, status)
+
+    def decode_int8():
+        pkv.pkv_paged_decode_int8(out, q, kc, vc, ks, vs, bt, cl, mcl, w.softmax_scale, ws_t,
+                                  status)
+
+    def decode_fp16():
+        pkv.pkv_paged_decode_fp16(out, q, kf, vf, bt, cl, mcl, w.softmax_scale, ws_t, status)
+
+    for _ in range(args.warmup):
+        step_int8()
+        decode_int8()
+        decode_fp16()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step_int8()
+        ev[i][1].record(stream)
+        decode_int8()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([total_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # fp16 decode of the same batch (reported as a variant)
+    Kf = min(K, 500)
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kf)]
+    for i in range(Kf):
+        flush.zero_()
+        evf[i][0].record(stream)
+        decode_fp16()
+        evf[i][1].record(stream)
+    torch.cuda.synchronize()
+    f16_ms = [e[0].elapsed_time(e[1]) for e in evf]
+
+    # end to end through the public API with host buffers: per step the
+    # query, block tables, context lengths and tail ids go host -> device and
+    # the output comes back
+    hq_pin = torch.from_numpy(w.query).pin_memory()
+    hbt_pin = torch.from_numpy(w.block_tables).pin_memory()
+    hcl_pin = torch.from_numpy(w.context_lens).pin_memory()
+    htl_pin = torch.from_numpy(tails_np).pin_memory()
+    hout = torch.empty((n, hq, d), dtype=torch.float32).pin_memory()
+    Ke = min(K, 500)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for i in range(Ke):
+        flush.zero_()
+        e0.record(stream)
+        q.copy_(hq_pin, non_blocking=True)
+        bt.copy_(hbt_pin, non_blocking=True)
+        cl.copy_(hcl_pin, non_blocking=True)
+        tails.copy_(htl_pin, non_blocking=True)
+        step_int8()
+        decode_int8()
+        hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    h2d = (w.query.nbytes + w.block_tables.nbytes + w.context_lens.nbytes + tails_np.nbytes)
+    d2h = n * hq * d * 4
+    st_val = int(status.item())
+
+    ntiles = len(tails_np) * hkv
+    dec_b = decode_bytes(w.context_lens, hkv, d, 1, True)
+    step_b = dec_b + quantize_bytes(ntiles, d)
+    f16_b = decode_bytes(w.context_lens, hkv, d, 2, False)
+    value = step_b * K * ws / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    dec_avg_ms = statistics.mean(dec_ms)
+    achieved = dec_b / (dec_avg_ms * 1e-3) / 1e9
+    traffic = TRAFFIC.get("decode_int8")
+    if traffic is not None and traffic[1] != _src_hash():
+        traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8-kv f16-mma f32-acc",
+        "data": "synthetic",
+        "config": {"workload": f"{CONFIG}: {n} seqs x ctx {mcl}, {hq} q / {hkv} kv heads, "
+                               f"head_dim {d}, block 16, pool {w.num_blocks} blocks; step = "
+                               f"INT8 quantize of {len(tails_np)} tail blocks + INT8 decode",
+                   "l2": "flushed between steps (256 MiB write, outside the events)",
+                   "parallelism": f"weak: the batch replicated per GPU x{ws}"},
+        "seq_steps_per_s": n * K * ws / (total_ms * 1e-3),
+        "p50_us_per_step": 1e3 * statistics.median(step_ms),
+        "p90_us_per_step": 1e3 * float(np.percentile(step_ms, 90)),
+        "pct_hbm_peak": 100.0 * value / ws / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "kernel": "INT8 decode call (decode + reduce kernels), "
+                               f"{dec_b} algorithmic bytes per call",
+                     "traffic": None if traffic is None else traffic[0]},
+        "variants": {
+            "decode_fp16": {"p50_us": 1e3 * statistics.median(f16_ms),
+                            "GB/s": f16_b / (statistics.mean(f16_ms) * 1e-3) / 1e9,
+                            "frac_of_peak": f16_b / (statistics.mean(f16_ms) * 1e-3) / 1e9 / peak,
+                            "bytes": f16_b},
+            "decode_int8": {"p50_us": 1e3 * statistics.median(dec_ms), "GB/s": achieved,
+                            "bytes": dec_b},
+        },
+        "e2e": {"value": step_b * Ke / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": 3 * K,
+        "dev_status": st_val,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

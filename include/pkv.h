@@ -41,6 +41,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -85,7 +91,7 @@ typedef enum pkv_status {
  *   dev_status         optional device int32 (may be NULL)
  *   stream             cudaStream_t as void*
  */
-pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16,
+PKV_API pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16,
                                int8_t *k_codes, int8_t *v_codes,
                                float *k_scales, float *v_scales,
                                const int32_t *block_ids, int num_ids,
@@ -121,7 +127,7 @@ pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16,
  * Two calls sharing a workspace must not overlap on the GPU.
  * num_seqs == 0 returns PKV_OK without launching.
  */
-pkv_status pkv_paged_decode_fp16(float *out, const void *query,
+PKV_API pkv_status pkv_paged_decode_fp16(float *out, const void *query,
                                  const void *k_cache, const void *v_cache,
                                  int num_blocks, const int32_t *block_tables,
                                  int max_blocks_per_seq,
@@ -141,7 +147,7 @@ pkv_status pkv_paged_decode_fp16(float *out, const void *query,
  *   k_codes/v_codes  int8 pools, 16-byte aligned
  *   k_scales/v_scales fp32 [num_blocks][num_kv_heads], 4-byte aligned
  */
-pkv_status pkv_paged_decode_int8(float *out, const void *query,
+PKV_API pkv_status pkv_paged_decode_int8(float *out, const void *query,
                                  const int8_t *k_codes, const int8_t *v_codes,
                                  const float *k_scales, const float *v_scales,
                                  int num_blocks, const int32_t *block_tables,
@@ -157,7 +163,7 @@ pkv_status pkv_paged_decode_int8(float *out, const void *query,
  * Bytes of workspace a decode call with these sizes needs (either variant).
  * Pure host arithmetic: no CUDA call.  Returns 0 for invalid sizes.
  */
-size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                  int head_dim, int max_context_len);
 
 /*
@@ -166,10 +172,10 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
  * partial result that the split-context reduce merges).  0 restores the
  * automatic choice (every resident warp of the device).  Process-wide.
  */
-pkv_status pkv_set_decode_workers(int max_workers);
+PKV_API pkv_status pkv_set_decode_workers(int max_workers);
 
 /* Static description of a status code. */
-const char *pkv_status_string(pkv_status status);
+PKV_API const char *pkv_status_string(pkv_status status);
 
 #ifdef __cplusplus
 }

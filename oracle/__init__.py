@@ -153,19 +153,25 @@ def decode_int8(query, k_codes, v_codes, k_scales, v_scales, block_tables,
                    softmax_scale, num_threads, return_flags)
 
 
-def quantize(pool, block_ids=None, code_pool=None, scales=None):
+def quantize(pool, block_ids=None, code_pool=None, scales=None, inplace=False):
     """Symmetric per-(block, kv-head) INT8 quantization of an fp16 pool.
 
     pool [NB][Hkv][B][d] fp16.  block_ids: optional int32 ids (duplicates
     allowed); None means every block.  Returns (codes int8 like pool,
     scales float32 [NB][Hkv]); tiles not named by block_ids keep the values of
-    ``code_pool`` / ``scales`` when given, else zeros.
+    ``code_pool`` / ``scales`` when given, else zeros.  With ``inplace`` the
+    given (contiguous) ``code_pool`` and ``scales`` arrays are written.
     """
     lib = _load()
     x = _c(pool, np.float16)
     nb, hkv, bs, d = x.shape
-    codes = np.zeros(x.shape, np.int8) if code_pool is None else _c(code_pool, np.int8).copy()
-    sc = np.zeros((nb, hkv), np.float32) if scales is None else _c(scales, np.float32).copy()
+    if inplace:
+        codes, sc = code_pool, scales
+        assert codes.flags.c_contiguous and codes.dtype == np.int8 and codes.shape == x.shape
+        assert sc.flags.c_contiguous and sc.dtype == np.float32 and sc.shape == (nb, hkv)
+    else:
+        codes = np.zeros(x.shape, np.int8) if code_pool is None else _c(code_pool, np.int8).copy()
+        sc = np.zeros((nb, hkv), np.float32) if scales is None else _c(scales, np.float32).copy()
     ids = None if block_ids is None else _c(block_ids, np.int32).reshape(-1)
     nids = 0 if ids is None else ids.size
     bad = lib.pkv_oracle_quantize(_ptr(codes), _ptr(sc), _ptr(x), _ptr(ids), nids,

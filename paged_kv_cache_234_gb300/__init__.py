@@ -1,0 +1,193 @@
+"""Python binding of libpkv: paged decode attention (fp16 / INT8 KV) for GB300.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of ``libpkv.so`` behind the C ABI declared in ``include/pkv.h``;
+PyTorch supplies device memory and streams.  There is no fallback: if the
+library has not been built (``paged_kv_cache_234_gb300.build.build()``), every
+call raises.
+
+The functions carry the C names and take torch tensors:
+
+* ``pkv_quantize_blocks``     fp16 K/V tiles -> INT8 codes + fp32 scales
+* ``pkv_paged_decode_fp16``   decode-step attention over fp16 K/V pools
+* ``pkv_paged_decode_int8``   decode-step attention over INT8 K/V pools
+* ``pkv_decode_workspace_size``, ``pkv_set_decode_workers``,
+  ``pkv_status_string``
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "_build", "libpkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = 1
+PKV_ERR_UNSUPPORTED = 2
+PKV_ERR_MISALIGNED = 3
+PKV_ERR_WORKSPACE = 4
+PKV_ERR_CUDA = 5
+
+PKV_DEV_BAD_BLOCK = 1
+PKV_DEV_BAD_CTX = 2
+PKV_DEV_TIMEOUT = 4
+
+EXPORTED = ("pkv_quantize_blocks", "pkv_paged_decode_fp16", "pkv_paged_decode_int8",
+            "pkv_decode_workspace_size", "pkv_set_decode_workers", "pkv_status_string")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {pkv_status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library with argument types set (raises if not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libpkv is not built ({LIB_PATH} missing); run "
+                "paged_kv_cache_234_gb300.build.build() first -- there is no fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.pkv_quantize_blocks.restype = I
+        L.pkv_quantize_blocks.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P]
+        dec = [P, P, P, P, I, P, I, P, I, I, I, I, I, I, F, P, Z, P, P]
+        L.pkv_paged_decode_fp16.restype = I
+        L.pkv_paged_decode_fp16.argtypes = dec
+        L.pkv_paged_decode_int8.restype = I
+        L.pkv_paged_decode_int8.argtypes = dec[:4] + [P, P] + dec[4:]
+        L.pkv_decode_workspace_size.restype = Z
+        L.pkv_decode_workspace_size.argtypes = [I, I, I, I, I]
+        L.pkv_set_decode_workers.restype = I
+        L.pkv_set_decode_workers.argtypes = [I]
+        L.pkv_status_string.restype = ctypes.c_char_p
+        L.pkv_status_string.argtypes = [I]
+        _lib = L
+        return L
+
+
+def pkv_status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(t, name, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len) -> int:
+    return int(lib().pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                               max_context_len))
+
+
+def pkv_set_decode_workers(max_workers: int) -> None:
+    st = lib().pkv_set_decode_workers(int(max_workers))
+    if st != PKV_OK:
+        raise PkvError(st, "pkv_set_decode_workers")
+
+
+def pkv_quantize_blocks(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
+                        block_ids=None, dev_status=None, stream=None) -> None:
+    """Quantize the (block, kv head) tiles of fp16 pools [NB][Hkv][16][d]."""
+    import torch
+    _check(k_fp16, "k_fp16", torch.float16)
+    _check(v_fp16, "v_fp16", torch.float16)
+    _check(k_codes, "k_codes", torch.int8)
+    _check(v_codes, "v_codes", torch.int8)
+    _check(k_scales, "k_scales", torch.float32)
+    _check(v_scales, "v_scales", torch.float32)
+    _check(block_ids, "block_ids", torch.int32)
+    _check(dev_status, "dev_status", torch.int32)
+    nb, hkv, bs, d = k_fp16.shape
+    nids = 0 if block_ids is None else block_ids.numel()
+    st = lib().pkv_quantize_blocks(
+        _ptr(k_fp16), _ptr(v_fp16), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+        _ptr(v_scales), _ptr(block_ids), nids, nb, hkv, d, bs, _ptr(dev_status),
+        _stream(stream))
+    if st != PKV_OK:
+        raise PkvError(st, "pkv_quantize_blocks")
+
+
+def _decode(fn_name, out, query, kp, vp, ks, vs, block_tables, context_lens,
+            max_context_len, softmax_scale, workspace, dev_status, stream):
+    import torch
+    _check(out, "out", torch.float32)
+    _check(query, "query", torch.float16)
+    _check(block_tables, "block_tables", torch.int32)
+    _check(context_lens, "context_lens", torch.int32)
+    _check(workspace, "workspace")
+    _check(dev_status, "dev_status", torch.int32)
+    n, hq, d = query.shape
+    nb, hkv, bs, _ = kp.shape
+    mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = [_ptr(out), _ptr(query), _ptr(kp), _ptr(vp)]
+    if ks is not None:
+        args += [_ptr(ks), _ptr(vs)]
+    args += [nb, _ptr(block_tables), mb, _ptr(context_lens), int(max_context_len), n, hq, hkv,
+             d, bs, float(softmax_scale), _ptr(workspace), ws_bytes, _ptr(dev_status),
+             _stream(stream)]
+    st = getattr(lib(), fn_name)(*args)
+    if st != PKV_OK:
+        raise PkvError(st, fn_name)
+
+
+def pkv_paged_decode_fp16(out, query, k_cache, v_cache, block_tables, context_lens,
+                          max_context_len, softmax_scale, workspace, dev_status=None,
+                          stream=None) -> None:
+    """out[N][Hq][d] fp32 = decode attention of query over fp16 pools."""
+    import torch
+    _check(k_cache, "k_cache", torch.float16)
+    _check(v_cache, "v_cache", torch.float16)
+    _decode("pkv_paged_decode_fp16", out, query, k_cache, v_cache, None, None, block_tables,
+            context_lens, max_context_len, softmax_scale, workspace, dev_status, stream)
+
+
+def pkv_paged_decode_int8(out, query, k_codes, v_codes, k_scales, v_scales, block_tables,
+                          context_lens, max_context_len, softmax_scale, workspace,
+                          dev_status=None, stream=None) -> None:
+    """out[N][Hq][d] fp32 = decode attention of query over INT8 pools + scales."""
+    import torch
+    _check(k_codes, "k_codes", torch.int8)
+    _check(v_codes, "v_codes", torch.int8)
+    _check(k_scales, "k_scales", torch.float32)
+    _check(v_scales, "v_scales", torch.float32)
+    _decode("pkv_paged_decode_int8", out, query, k_codes, v_codes, k_scales, v_scales,
+            block_tables, context_lens, max_context_len, softmax_scale, workspace, dev_status,
+            stream)
+
+
+def decode_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, device=None):
+    """A uint8 CUDA tensor big enough to serve as a decode workspace."""
+    import torch
+    nbytes = pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                       max_context_len)
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device or "cuda")

@@ -1,0 +1,886 @@
+// pkv_decode.cu -- decode-step paged attention over a block-table-indexed KV
+// cache, fp16 or INT8 KV, for sm_103a.
+//
+// What is computed (PagedKV-Fusion README, "Architecture": online softmax,
+// GQA, per-(block, head) INT8; paged-attention-runtime summary, CORE
+// CAPABILITIES 2: block-table indirection, online single-pass softmax, FP32
+// accumulation; "PagedAttention & KV-Cache Memory Management" section 2.1:
+// block = table[t / 16], slot = t % 16):
+//   out[s][h] = sum_t softmax_t(scale * <q[s][h], K_t>) V_t,  t < ctx[s],
+// with query head h reading kv head h / (Hq / Hkv).
+//
+// Work decomposition.  A work item is (sequence, kv head, group of up to 8
+// query heads of that kv head); its pages are the sequence's 16-token
+// blocks.  All items' pages form one stream of T pages, and every warp of a
+// persistent grid (one worker per resident warp) streams one contiguous,
+// equal share of it.  A worker's share is therefore a run of "pieces": at
+// most one partial item at each end and whole items in between.  Whole items
+// are finished in place; partial pieces leave (running max, running sum,
+// unnormalised accumulator) in the workspace, and the split-context reduce
+// kernel merges the pieces of each split item.  This gives every SM the same
+// number of bytes whatever the mix of context lengths.
+//
+// Per worker (warp), pages flow through a private ring of S shared-memory
+// stages.  Lane 0 issues TMA tile loads (16 rows x head_dim, 128- or 64-byte
+// swizzled) for the K and V tiles of a page, plus 4-byte cp.async copies of
+// the two INT8 scales, all completing on the stage's mbarrier; the ring
+// keeps S pages in flight while the warp computes on the oldest one.
+//
+// Per page, the GQA group's query heads (up to 8) share one read of K and V:
+//   S^T[16 tok][8 heads] = K_page[16 x d] . Q^T      (m16n8k16, f16 -> f32)
+//   online softmax in base 2 (scores pre-multiplied by scale*log2 e)
+//   O^T[d][8 heads]     += V_page^T[d x 16] . P^T    (m16n8k16, f16 -> f32)
+// INT8 codes are widened to f16 exactly (byte-permute into 1024 + code + 128,
+// subtract 1152); the K scale multiplies the scores and the V scale the
+// probabilities, so dequantisation costs one multiply per score.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pkv_host.cuh"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarps = 4;  // workers per CTA
+constexpr int kThreads = kWarps * 32;
+constexpr int kPage = 16;              // tokens per block
+constexpr int kItemHeads = 8;          // query heads per work item (mma N)
+constexpr int kMaxWorkers = 4096;      // workspace is sized for at most this many
+constexpr int kMaxSeqs = 8192;         // per-sequence tables live in shared memory
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
+
+int g_worker_cap = 0;  // pkv_set_decode_workers
+std::mutex g_cfg_mu;
+
+struct DecodeArgs {
+    float *out;
+    const __half *query;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const float *k_scales;
+    const float *v_scales;
+    float *partials;  // [num_workers * 2][rec_heads][head_dim + 4]
+    int32_t *dev_status;
+    int num_seqs, num_heads, num_kv_heads;
+    int group;           // query heads per kv head
+    int qgroups;         // ceil(group / 8)
+    int items_per_seq;   // num_kv_heads * qgroups
+    int rec_heads;       // min(8, group): heads per partial record
+    int max_blocks_per_seq;
+    int num_blocks;
+    int ctx_cap;         // largest valid context length
+    int num_workers;
+    float scale_log2;    // softmax_scale * log2(e)
+};
+
+template <bool kInt8, int kD>
+struct Cfg {
+    static constexpr int kElem = kInt8 ? 1 : 2;
+    static constexpr int kRowBytes = kD * kElem;                 // 256 / 128 / 64
+    static constexpr int kTileBytes = kPage * kRowBytes;         // one (block, kv head) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;           // K tile + V tile
+    static constexpr int kBoxInner = kRowBytes > 128 ? 128 / kElem : kD;  // elements
+    static constexpr int kBoxes = kD / kBoxInner;
+    static constexpr int kBoxBytes = kPage * kBoxInner * kElem;
+    static constexpr int kSwizzle = kRowBytes >= 128 ? 128 : 64;
+    static constexpr int kStages = kStageBytes >= 8192 ? 3 : kStageBytes >= 4096 ? 4 : 6;
+    static constexpr int kStageRegion = kWarps * kStages * kStageBytes;
+    static constexpr int kHdrOffset = kStageRegion;                         // 16 B per stage
+    static constexpr int kBarOffset = kHdrOffset + kWarps * kStages * 16;   // 8 B per stage
+    static constexpr int kTabOffset = kBarOffset + kWarps * kStages * 8;
+    static size_t smem_bytes(int num_seqs)
+    {
+        return 1024 + kTabOffset + static_cast<size_t>(2 * num_seqs + 1) * sizeof(int32_t);
+    }
+};
+
+// Byte offset of 16-byte chunk `ch` of row `t` inside a TMA-written tile.
+// Rows wider than 128 bytes arrive as 128-byte-wide boxes of 16 rows each.
+template <int kRowBytes>
+__device__ __forceinline__ uint32_t swz(int t, int ch)
+{
+    if constexpr (kRowBytes == 256) {
+        return ((ch >> 3) << 11) + (t << 7) + (((ch & 7) ^ (t & 7)) << 4);
+    } else if constexpr (kRowBytes == 128) {
+        return (t << 7) + (((ch) ^ (t & 7)) << 4);
+    } else {
+        return (t << 6) + (((ch) ^ ((t >> 1) & 3)) << 4);
+    }
+}
+
+// ------------------------------------------------------ per-sequence tables
+// ctxs[s]   = context length, or -1 if it is outside [0, ctx_cap]
+// prefix[s] = pages of all sequences before s (exclusive prefix sum)
+__device__ void build_page_tables(const DecodeArgs &p, int32_t *prefix, int32_t *ctxs)
+{
+    __shared__ int32_t warp_sums[kWarps];
+    __shared__ int32_t carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        carry = 0;
+        prefix[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < p.num_seqs; base += kThreads) {
+        const int s = base + threadIdx.x;
+        int np = 0;
+        if (s < p.num_seqs) {
+            const int c = p.context_lens[s];
+            const bool ok = c >= 0 && c <= p.ctx_cap;
+            ctxs[s] = ok ? c : -1;
+            np = ok ? (c + kPage - 1) / kPage : 0;
+        }
+        int v = np;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += n;
+        }
+        if (lane == 31) warp_sums[warp] = v;
+        __syncthreads();
+        int before = carry;
+        for (int j = 0; j < warp; ++j) before += warp_sums[j];
+        const int incl = before + v;
+        if (s < p.num_seqs) prefix[s + 1] = incl;
+        __syncthreads();
+        if (threadIdx.x == kThreads - 1) carry = incl;
+        __syncthreads();
+    }
+}
+
+// Position of one page in the stream of all items' pages.
+struct PageCursor {
+    int seq;     // sequence
+    int item;    // kv head * qgroups + query-head group
+    int page;    // page (16-token block) within the sequence
+    int npages;  // pages of the sequence
+
+    __device__ void seek(const DecodeArgs &p, const int32_t *prefix, int64_t x)
+    {
+        int lo = 0, hi = p.num_seqs;  // largest s with items_per_seq * prefix[s] <= x
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (static_cast<int64_t>(p.items_per_seq) * prefix[mid] <= x)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        seq = lo;
+        npages = prefix[lo + 1] - prefix[lo];
+        const int64_t r = x - static_cast<int64_t>(p.items_per_seq) * prefix[lo];
+        item = static_cast<int>(r / npages);
+        page = static_cast<int>(r % npages);
+    }
+
+    __device__ void next(const DecodeArgs &p, const int32_t *prefix)
+    {
+        if (++page < npages) return;
+        page = 0;
+        if (++item < p.items_per_seq) return;
+        item = 0;
+        do {
+            ++seq;
+        } while (seq < p.num_seqs && prefix[seq + 1] == prefix[seq]);
+        npages = seq < p.num_seqs ? prefix[seq + 1] - prefix[seq] : 0;
+    }
+};
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// exact int8 -> f16 pair: bytes (c + 128) under exponent 0x64 give 1024 + c + 128
+__device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t biased_word, uint32_t sel)
+{
+    const uint32_t h = ptx::prmt(biased_word, 0x64646464u, sel);
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+
+// Which worker's page range holds stream page x (largest w with a_w <= x).
+__device__ __forceinline__ int64_t worker_of(int64_t x, int64_t total, int workers)
+{
+    return ((x + 1) * workers - 1) / total;
+}
+
+template <bool kInt8, int kD>
+__global__ void __launch_bounds__(kThreads)
+    decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv)
+{
+    using C = Cfg<kInt8, kD>;
+    constexpr int S = C::kStages;
+    constexpr int KS = kD / 16;  // mma k-steps over head_dim, also m-tiles of O^T
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + C::kTabOffset);
+    int32_t *ctxs = prefix + p.num_seqs + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;  // mma fragment row group / column pair
+
+    if (threadIdx.x == 0) {
+        ptx::prefetch_tmap(&tmk);
+        ptx::prefetch_tmap(&tmv);
+    }
+    build_page_tables(p, prefix, ctxs);
+    const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
+
+    // Sequences with no pages: zero output (bad lengths are also reported).
+    for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x) {
+        if (prefix[s + 1] != prefix[s]) continue;
+        if (ctxs[s] < 0 && threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, PKV_DEV_BAD_CTX);
+        float4 *o = reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(s) * p.num_heads * kD);
+        for (int i = threadIdx.x; i < p.num_heads * kD / 4; i += kThreads)
+            o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    const int w = blockIdx.x * kWarps + warp;
+    if (w >= p.num_workers || total == 0) return;
+    const int64_t a = w * total / p.num_workers;
+    const int64_t b = (w + 1) * total / p.num_workers;
+    if (a >= b) return;
+    const int64_t n = b - a;
+
+    const uint32_t stage0 = ptx::smem_addr(smem) + warp * S * C::kStageBytes;
+    const uint32_t hdr0 = ptx::smem_addr(smem + C::kHdrOffset) + warp * S * 16;
+    int32_t *hdr_bad = reinterpret_cast<int32_t *>(smem + C::kHdrOffset) + warp * S * 4;
+    const float *hdr_f = reinterpret_cast<const float *>(hdr_bad);
+    const uint32_t bar0 = ptx::smem_addr(smem + C::kBarOffset) + warp * S * 8;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) ptx::mbar_init(bar0 + 8 * s, kInt8 ? 2 : 1);
+        ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    const uint64_t policy = ptx::policy_evict_first();
+    const int64_t mb = p.max_blocks_per_seq;
+
+    // Lane 0: start the copies of one page into stage `slot`.
+    auto issue = [&](int slot, int32_t blk, int kvh) {
+        const uint32_t bar = bar0 + 8 * slot;
+        if (blk < 0 || blk >= p.num_blocks) {
+            hdr_bad[slot * 4] = 1;
+            if (p.dev_status) atomicOr(p.dev_status, PKV_DEV_BAD_BLOCK);
+            ptx::mbar_arrive(bar);
+            if (kInt8) ptx::mbar_arrive(bar);
+            return;
+        }
+        hdr_bad[slot * 4] = 0;
+        ptx::mbar_arrive_expect_tx(bar, C::kStageBytes);
+        const int row = (blk * p.num_kv_heads + kvh) * kPage;
+        const uint32_t kdst = stage0 + slot * C::kStageBytes;
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+            ptx::tma_load_2d(kdst + bx * C::kBoxBytes, &tmk, bx * C::kBoxInner, row, bar, policy);
+            ptx::tma_load_2d(kdst + C::kTileBytes + bx * C::kBoxBytes, &tmv, bx * C::kBoxInner, row,
+                             bar, policy);
+        }
+        if constexpr (kInt8) {
+            const int64_t si = static_cast<int64_t>(blk) * p.num_kv_heads + kvh;
+            ptx::cp_async_4(hdr0 + slot * 16 + 4, p.k_scales + si);
+            ptx::cp_async_4(hdr0 + slot * 16 + 8, p.v_scales + si);
+            ptx::cp_async_arrive_noinc(bar);
+        }
+    };
+
+    // ---- prologue: block ids of the first pages, one lane each, then issue
+    PageCursor ci;
+    ci.seek(p, prefix, a);
+    PageCursor cc = ci;
+    const int pro = static_cast<int>(n < S ? n : S);
+    {
+        PageCursor cj = ci;
+        for (int j = 0; j < lane && j < pro - 1; ++j) cj.next(p, prefix);
+        const int32_t myblk =
+            lane < pro ? __ldg(p.block_tables + cj.seq * mb + cj.page) : 0;
+        const int mykvh = cj.item / p.qgroups;
+        for (int j = 0; j < pro; ++j) {
+            const int32_t blk = __shfl_sync(0xffffffffu, myblk, j);
+            const int kvh = __shfl_sync(0xffffffffu, mykvh, j);
+            if (lane == 0) issue(j, blk, kvh);
+        }
+        for (int j = 0; j < pro; ++j) ci.next(p, prefix);
+    }
+    int32_t nblk = 0;  // lane 0: block id of the next page to issue
+    if (lane == 0 && pro < n) nblk = __ldg(p.block_tables + ci.seq * mb + ci.page);
+
+    // ---- per-piece state
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 units), heads 2c and 2c+1
+    float l0 = 0.f, l1 = 0.f;              // lane-partial running sums
+    float o[KS][4];                        // O^T accumulators (see the output mapping)
+    uint32_t qf[KS][2];                    // Q^T B-fragments
+    bool piece_bad = false;
+    bool piece_has_a = true;
+    int piece_first_page = 0;
+
+    for (int64_t k = 0; k < n; ++k) {
+        const int slot = static_cast<int>(k % S);
+        const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
+        const bool first = (k == 0) || (cc.page == 0);
+        const bool last = (k == n - 1) || (cc.page == cc.npages - 1);
+        const int kvh = cc.item / p.qgroups;
+        const int qg = cc.item - kvh * p.qgroups;
+        const int h0 = kvh * p.group + qg * kItemHeads;
+        const int gh = min(kItemHeads, p.group - qg * kItemHeads);
+
+        if (first) {
+            // query fragments of the item's heads; heads past gh are zero
+            const __half *qrow = p.query + (static_cast<int64_t>(cc.seq) * p.num_heads + h0 + g) * kD;
+            const bool live = g < gh;
+            if constexpr (kInt8) {
+                // lane (g, c) holds q[g][DG*c .. DG*c + DG), DG = kD / 4
+                constexpr int DG = kD / 4;
+                uint4 qv[DG / 8];
+#pragma unroll
+                for (int j = 0; j < DG / 8; ++j)
+                    qv[j] = live ? __ldg(reinterpret_cast<const uint4 *>(qrow + DG * c) + j)
+                                 : make_uint4(0, 0, 0, 0);
+                const uint32_t *qw = reinterpret_cast<const uint32_t *>(qv);
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    qf[s][0] = qw[2 * s];
+                    qf[s][1] = qw[2 * s + 1];
+                }
+            } else {
+                const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    qf[s][0] = live ? __ldg(qw + 8 * s + c) : 0u;
+                    qf[s][1] = live ? __ldg(qw + 8 * s + 4 + c) : 0u;
+                }
+            }
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            piece_bad = false;
+            piece_has_a = (k == 0);
+            piece_first_page = cc.page;
+        }
+
+        // every lane waits (acquire); the outcome is made warp-uniform
+        const bool landed = ptx::mbar_wait_bounded(bar0 + 8 * slot, parity, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, landed)) {
+            // The copy never landed: report, let the other copies of this
+            // worker land (bounded), and stop this worker.
+            if (lane == 0 && p.dev_status) atomicOr(p.dev_status, PKV_DEV_TIMEOUT);
+            for (int64_t r = k + 1; r < n && r < k + S; ++r)
+                ptx::mbar_wait_bounded(bar0 + 8 * static_cast<int>(r % S),
+                                       static_cast<uint32_t>((r / S) & 1), kWaitLimitNs);
+            return;
+        }
+
+        if (hdr_bad[slot * 4]) {
+            piece_bad = true;
+        } else {
+            const int ntok = min(kPage, ctxs[cc.seq] - cc.page * kPage);
+            const uint32_t kt = stage0 + slot * C::kStageBytes;
+            const uint32_t vt = kt + C::kTileBytes;
+            float sk = 1.f, sv = 1.f;
+            if constexpr (kInt8) {
+                sk = hdr_f[slot * 4 + 1];
+                sv = hdr_f[slot * 4 + 2];
+            }
+
+            // ---- S^T = K_page . Q^T   (rows: tokens, cols: heads)
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (!kInt8) {
+                const int lt = (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int lch = lane >> 4;
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    uint32_t a0, a1, a2, a3;
+                    ptx::ldsm_x4(kt + swz<C::kRowBytes>(lt, 2 * s + lch), a0, a1, a2, a3);
+                    if (s & 1)
+                        ptx::mma_16816(sb, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                    else
+                        ptx::mma_16816(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                }
+            } else {
+                // lane (g, c): rows g and g+8, bytes [DG*c, DG*c + DG) with DG = kD/4
+                constexpr int CH = kD / 64;  // 16-byte chunks per row per lane
+                uint32_t kw[2][4 * CH];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        const uint4 v = ptx::lds128(kt + swz<C::kRowBytes>(g + 8 * r, CH * c + j));
+                        kw[r][4 * j + 0] = v.x ^ 0x80808080u;
+                        kw[r][4 * j + 1] = v.y ^ 0x80808080u;
+                        kw[r][4 * j + 2] = v.z ^ 0x80808080u;
+                        kw[r][4 * j + 3] = v.w ^ 0x80808080u;
+                    }
+                }
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    const uint32_t a0 = i8pair_to_h2(kw[0][s], 0x4140u);
+                    const uint32_t a2 = i8pair_to_h2(kw[0][s], 0x4342u);
+                    const uint32_t a1 = i8pair_to_h2(kw[1][s], 0x4140u);
+                    const uint32_t a3 = i8pair_to_h2(kw[1][s], 0x4342u);
+                    if (s & 1)
+                        ptx::mma_16816(sb, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                    else
+                        ptx::mma_16816(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                }
+            }
+
+            // ---- online softmax (base 2) over this page's tokens
+            const float sl = p.scale_log2 * sk;
+            float x0 = (sa[0] + sb[0]) * sl, x1 = (sa[1] + sb[1]) * sl;  // token g
+            float x2 = (sa[2] + sb[2]) * sl, x3 = (sa[3] + sb[3]) * sl;  // token g+8
+            if (ntok < kPage) {
+                if (g >= ntok) x0 = x1 = -INFINITY;
+                if (g + 8 >= ntok) x2 = x3 = -INFINITY;
+            }
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = ptx::ex2(m0 - mn0), al1 = ptx::ex2(m1 - mn1);
+            const float p0 = ptx::ex2(x0 - mn0), p1 = ptx::ex2(x1 - mn1);
+            const float p2 = ptx::ex2(x2 - mn0), p3 = ptx::ex2(x3 - mn1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            m0 = mn0;
+            m1 = mn1;
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int i = 0; i < KS; ++i) {
+                    o[i][0] *= al0;
+                    o[i][1] *= al1;
+                    o[i][2] *= al0;
+                    o[i][3] *= al1;
+                }
+            }
+            // P^T as the B operand: transpose the two 8x8 halves of P
+            const uint32_t pb0 = ptx::movmatrix_t(pack_half2(p0 * sv, p1 * sv));
+            const uint32_t pb1 = ptx::movmatrix_t(pack_half2(p2 * sv, p3 * sv));
+
+            // ---- O^T += V_page^T . P^T
+            if constexpr (!kInt8) {
+                const int lt = (lane & 7) + 8 * (lane >> 4);
+                const int lch = (lane >> 3) & 1;
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (ntok < kPage) {  // NaN-safe: zero V rows of tokens past the end
+                    mlo = (2 * c < ntok ? 0x0000ffffu : 0u) | (2 * c + 1 < ntok ? 0xffff0000u : 0u);
+                    mhi = (2 * c + 8 < ntok ? 0x0000ffffu : 0u) |
+                          (2 * c + 9 < ntok ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < KS; ++i) {
+                    uint32_t a0, a1, a2, a3;
+                    ptx::ldsm_x4_t(vt + swz<C::kRowBytes>(lt, 2 * i + lch), a0, a1, a2, a3);
+                    ptx::mma_16816(o[i], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+                }
+            } else {
+                // lane (g, c): tokens 2c, 2c+1, 2c+8, 2c+9; bytes [DG*g, DG*g + DG), DG = kD/8
+                constexpr int NW = kD / 32;  // words per token per lane
+                uint32_t vw[4][NW];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int t = 2 * c + (r & 1) + 8 * (r >> 1);
+                    if constexpr (kD == 128) {
+                        const uint4 v = ptx::lds128(vt + swz<C::kRowBytes>(t, g));
+                        vw[r][0] = v.x ^ 0x80808080u;
+                        vw[r][1] = v.y ^ 0x80808080u;
+                        vw[r][2] = v.z ^ 0x80808080u;
+                        vw[r][3] = v.w ^ 0x80808080u;
+                    } else {
+                        const uint2 v = ptx::lds64(vt + swz<C::kRowBytes>(t, g >> 1) + (g & 1) * 8);
+                        vw[r][0] = v.x ^ 0x80808080u;
+                        vw[r][1] = v.y ^ 0x80808080u;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < KS; ++i) {
+                    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+                    const uint32_t il01 = ptx::prmt(vw[0][i >> 1], vw[1][i >> 1], sel);
+                    const uint32_t il23 = ptx::prmt(vw[2][i >> 1], vw[3][i >> 1], sel);
+                    ptx::mma_16816(o[i], i8pair_to_h2(il01, 0x4140u), i8pair_to_h2(il01, 0x4342u),
+                                   i8pair_to_h2(il23, 0x4140u), i8pair_to_h2(il23, 0x4342u), pb0,
+                                   pb1);
+                }
+            }
+        }
+        __syncwarp();
+
+        // ---- refill this stage with the page S ahead
+        if (k + S < n) {
+            if (lane == 0) {
+                ptx::fence_proxy_async_smem();
+                issue(slot, nblk, ci.item / p.qgroups);
+            }
+            ci.next(p, prefix);
+            if (lane == 0 && k + S + 1 < n) nblk = __ldg(p.block_tables + ci.seq * mb + ci.page);
+        }
+
+        // ---- piece finished: final output, or a partial for the reduce
+        if (last) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            }
+            const bool whole = piece_first_page == 0 && cc.page == cc.npages - 1;
+            const int hA = 2 * c, hB = 2 * c + 1;
+            float *dstA, *dstB;
+            float fA, fB;
+            if (whole) {
+                const int64_t orow = (static_cast<int64_t>(cc.seq) * p.num_heads + h0) * kD;
+                dstA = p.out + orow + static_cast<int64_t>(hA) * kD;
+                dstB = p.out + orow + static_cast<int64_t>(hB) * kD;
+                fA = piece_bad ? 0.f : 1.f / l0;
+                fB = piece_bad ? 0.f : 1.f / l1;
+            } else {
+                const int slotp = piece_has_a ? 0 : 1;
+                float *rec = p.partials +
+                             (static_cast<int64_t>(w) * 2 + slotp) * p.rec_heads * (kD + 4);
+                dstA = rec + hA * (kD + 4) + 4;
+                dstB = rec + hB * (kD + 4) + 4;
+                fA = fB = 1.f;
+                if (g == 0) {
+                    if (hA < gh) {
+                        dstA[-4] = m0;
+                        dstA[-3] = piece_bad ? -1.f : l0;
+                    }
+                    if (hB < gh) {
+                        dstB[-4] = m1;
+                        dstB[-3] = piece_bad ? -1.f : l1;
+                    }
+                }
+            }
+            if (piece_bad) {
+#pragma unroll
+                for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            }
+            if constexpr (!kInt8) {
+#pragma unroll
+                for (int i = 0; i < KS; ++i) {
+                    if (hA < gh) {
+                        dstA[16 * i + g] = o[i][0] * fA;
+                        dstA[16 * i + 8 + g] = o[i][2] * fA;
+                    }
+                    if (hB < gh) {
+                        dstB[16 * i + g] = o[i][1] * fB;
+                        dstB[16 * i + 8 + g] = o[i][3] * fB;
+                    }
+                }
+            } else {
+                constexpr int DG = kD / 8;  // lane (g, c) owns d in [DG*g, DG*g + DG)
+#pragma unroll
+                for (int i = 0; i < KS; i += 2) {
+                    if (hA < gh)
+                        *reinterpret_cast<float4 *>(dstA + DG * g + 2 * i) =
+                            make_float4(o[i][0] * fA, o[i][2] * fA, o[i + 1][0] * fA,
+                                        o[i + 1][2] * fA);
+                    if (hB < gh)
+                        *reinterpret_cast<float4 *>(dstB + DG * g + 2 * i) =
+                            make_float4(o[i][1] * fB, o[i][3] * fB, o[i + 1][1] * fB,
+                                        o[i + 1][3] * fB);
+                }
+            }
+        }
+        cc.next(p, prefix);
+    }
+}
+
+// Split-context reduce: one warp per item that more than one worker touched.
+// out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w with M = max_w m_w;
+// a piece flagged bad (l < 0) zeroes the item.
+template <int kD>
+__global__ void __launch_bounds__(kThreads) reduce_kernel(const DecodeArgs p)
+{
+    extern __shared__ int32_t tabs[];
+    int32_t *prefix = tabs;
+    int32_t *ctxs = prefix + p.num_seqs + 1;
+    build_page_tables(p, prefix, ctxs);
+    const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t it = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    if (total == 0 || it >= static_cast<int64_t>(p.num_seqs) * p.items_per_seq) return;
+    const int seq = static_cast<int>(it / p.items_per_seq);
+    const int item = static_cast<int>(it % p.items_per_seq);
+    const int np = prefix[seq + 1] - prefix[seq];
+    if (np == 0) return;
+    const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[seq] +
+                       static_cast<int64_t>(item) * np;
+    const int64_t e0 = s0 + np;
+    const int W = p.num_workers;
+    const int64_t wf = worker_of(s0, total, W), wl = worker_of(e0 - 1, total, W);
+    if (wf == wl) return;  // finished in place by one worker
+    const int kvh = item / p.qgroups, qg = item - kvh * p.qgroups;
+    const int h0 = kvh * p.group + qg * kItemHeads;
+    const int gh = min(kItemHeads, p.group - qg * kItemHeads);
+    for (int h = 0; h < gh; ++h) {
+        float M = -INFINITY;
+        bool bad = false;
+        for (int64_t w = wf; w <= wl; ++w) {
+            const int64_t aw = w * total / W;
+            if (aw == (w + 1) * total / W) continue;  // worker with no pages
+            const int slot = s0 <= aw ? 0 : 1;
+            const float *rec = p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
+            M = fmaxf(M, rec[0]);
+            bad |= rec[1] < 0.f;
+        }
+        float acc[kD / 32];
+#pragma unroll
+        for (int j = 0; j < kD / 32; ++j) acc[j] = 0.f;
+        float L = 0.f;
+        for (int64_t w = wf; w <= wl; ++w) {
+            const int64_t aw = w * total / W;
+            if (aw == (w + 1) * total / W) continue;
+            const int slot = s0 <= aw ? 0 : 1;
+            const float *rec = p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
+            const float f = ptx::ex2(rec[0] - M);
+            L += f * rec[1];
+#pragma unroll
+            for (int j = 0; j < kD / 32; ++j) acc[j] += f * rec[4 + lane + 32 * j];
+        }
+        float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
+        const float inv = bad ? 0.f : 1.f / L;
+#pragma unroll
+        for (int j = 0; j < kD / 32; ++j) dst[lane + 32 * j] = bad ? 0.f : acc[j] * inv;
+    }
+}
+
+// ------------------------------------------------------------------- host
+struct DecodeCall {
+    float *out;
+    const void *query;
+    const void *kpool;
+    const void *vpool;
+    const float *k_scales;
+    const float *v_scales;
+    int num_blocks;
+    const int32_t *block_tables;
+    int max_blocks_per_seq;
+    const int32_t *context_lens;
+    int max_context_len;
+    int num_seqs, num_heads, num_kv_heads, head_dim, block_size;
+    float softmax_scale;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *dev_status;
+    void *stream;
+};
+
+struct Shape {
+    int group, qgroups, items_per_seq, rec_heads, ctx_cap;
+    int64_t max_pages;  // upper bound of the page stream length
+};
+
+pkv_status check_shape(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                       int max_context_len, int max_blocks_per_seq, Shape *sh)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_context_len < 0 || max_blocks_per_seq < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    sh->group = num_heads / num_kv_heads;
+    sh->qgroups = (sh->group + kItemHeads - 1) / kItemHeads;
+    const int64_t ips = static_cast<int64_t>(num_kv_heads) * sh->qgroups;
+    if (ips > (1 << 20)) return PKV_ERR_UNSUPPORTED;
+    sh->items_per_seq = static_cast<int>(ips);
+    sh->rec_heads = sh->group < kItemHeads ? sh->group : kItemHeads;
+    const int64_t cap_tab = static_cast<int64_t>(max_blocks_per_seq) * kPage;
+    sh->ctx_cap = static_cast<int>(max_context_len < cap_tab ? max_context_len : cap_tab);
+    const int64_t pages_per_seq = (sh->ctx_cap + kPage - 1) / kPage;
+    if (static_cast<int64_t>(num_seqs) * pages_per_seq > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    sh->max_pages = static_cast<int64_t>(num_seqs) * pages_per_seq * ips;
+    return PKV_OK;
+}
+
+size_t workspace_bytes_for(const Shape &sh, int head_dim)
+{
+    const int64_t workers = sh.max_pages < kMaxWorkers ? sh.max_pages : kMaxWorkers;
+    return static_cast<size_t>(workers) * 2 * sh.rec_heads * (head_dim + 4) * sizeof(float);
+}
+
+struct OccCache {
+    int device = -1;
+    size_t smem = 0;
+    int per_sm = 0;
+};
+
+template <bool kInt8, int kD>
+pkv_status launch(const DecodeCall &call, const Shape &sh)
+{
+    using C = Cfg<kInt8, kD>;
+    DeviceInfo di;
+    if (!current_device_info(&di)) return PKV_ERR_CUDA;
+    const size_t smem = C::smem_bytes(call.num_seqs);
+    if (smem > di.max_smem_optin) return PKV_ERR_UNSUPPORTED;
+    auto kern = decode_kernel<kInt8, kD>;
+    static OccCache occ[64];
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_cfg_mu);
+        OccCache &oc = occ[di.device & 63];
+        if (oc.device != di.device || oc.smem != smem) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess)
+                return PKV_ERR_CUDA;
+            int v = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, smem) !=
+                cudaSuccess)
+                return PKV_ERR_CUDA;
+            oc.device = di.device;
+            oc.smem = smem;
+            oc.per_sm = v;
+        }
+        per_sm = oc.per_sm;
+    }
+    if (per_sm <= 0) return PKV_ERR_UNSUPPORTED;
+    int64_t workers = static_cast<int64_t>(per_sm) * di.num_sms * kWarps;
+    if (workers > kMaxWorkers) workers = kMaxWorkers;
+    if (g_worker_cap > 0 && workers > g_worker_cap) workers = g_worker_cap;
+    if (workers > sh.max_pages) workers = sh.max_pages;
+    if (workers < 1) workers = 1;
+
+    CUtensorMap tmk, tmv;
+    const uint64_t rows = static_cast<uint64_t>(call.num_blocks) * call.num_kv_heads * kPage;
+    if (!encode_tmap_2d(&tmk, call.kpool, C::kElem, kD, rows, C::kBoxInner, kPage, C::kSwizzle) ||
+        !encode_tmap_2d(&tmv, call.vpool, C::kElem, kD, rows, C::kBoxInner, kPage, C::kSwizzle))
+        return PKV_ERR_CUDA;
+
+    DecodeArgs args;
+    args.out = call.out;
+    args.query = static_cast<const __half *>(call.query);
+    args.block_tables = call.block_tables;
+    args.context_lens = call.context_lens;
+    args.k_scales = call.k_scales;
+    args.v_scales = call.v_scales;
+    args.partials = static_cast<float *>(call.workspace);
+    args.dev_status = call.dev_status;
+    args.num_seqs = call.num_seqs;
+    args.num_heads = call.num_heads;
+    args.num_kv_heads = call.num_kv_heads;
+    args.group = sh.group;
+    args.qgroups = sh.qgroups;
+    args.items_per_seq = sh.items_per_seq;
+    args.rec_heads = sh.rec_heads;
+    args.max_blocks_per_seq = call.max_blocks_per_seq;
+    args.num_blocks = call.num_blocks;
+    args.ctx_cap = sh.ctx_cap;
+    args.num_workers = static_cast<int>(workers);
+    args.scale_log2 = call.softmax_scale * 1.4426950408889634f;
+
+    cudaStream_t st = static_cast<cudaStream_t>(call.stream);
+    const int grid = static_cast<int>((workers + kWarps - 1) / kWarps);
+    kern<<<grid, kThreads, smem, st>>>(args, tmk, tmv);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (workers > 1) {
+        const size_t rsmem = static_cast<size_t>(2 * call.num_seqs + 1) * sizeof(int32_t);
+        const int64_t items = static_cast<int64_t>(call.num_seqs) * sh.items_per_seq;
+        const int64_t rgrid = (items + kWarps - 1) / kWarps;
+        if (rgrid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+        auto rk = reduce_kernel<kD>;
+        if (rsmem > 48 * 1024 &&
+            cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(rsmem)) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        rk<<<static_cast<unsigned>(rgrid), kThreads, rsmem, st>>>(args);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+pkv_status decode_entry(const DecodeCall &call, bool int8)
+{
+    if (!call.out || !call.query || !call.kpool || !call.vpool || !call.block_tables ||
+        !call.context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (int8 && (!call.k_scales || !call.v_scales)) return PKV_ERR_INVALID_ARG;
+    if (call.num_blocks <= 0 || call.block_size <= 0) return PKV_ERR_INVALID_ARG;
+    if (!(call.softmax_scale == call.softmax_scale) || call.softmax_scale > 3.0e38f ||
+        call.softmax_scale < -3.0e38f)
+        return PKV_ERR_INVALID_ARG;
+    Shape sh;
+    const pkv_status st = check_shape(call.num_seqs, call.num_heads, call.num_kv_heads,
+                                      call.head_dim, call.max_context_len,
+                                      call.max_blocks_per_seq, &sh);
+    if (st != PKV_OK) return st;
+    if (call.block_size != kPage) return PKV_ERR_UNSUPPORTED;
+    if (call.num_seqs > kMaxSeqs) return PKV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(call.num_blocks) * call.num_kv_heads * kPage > 0x7fffffffLL)
+        return PKV_ERR_UNSUPPORTED;
+    if (!aligned(call.out, 16) || !aligned(call.query, 16) || !aligned(call.kpool, 16) ||
+        !aligned(call.vpool, 16) || !aligned(call.block_tables, 4) ||
+        !aligned(call.context_lens, 4) || (call.dev_status && !aligned(call.dev_status, 4)) ||
+        (int8 && (!aligned(call.k_scales, 4) || !aligned(call.v_scales, 4))))
+        return PKV_ERR_MISALIGNED;
+    if (call.num_seqs == 0) return PKV_OK;
+    const size_t need = workspace_bytes_for(sh, call.head_dim);
+    if (need > 0 && (!call.workspace || call.workspace_bytes < need)) return PKV_ERR_WORKSPACE;
+    if (call.workspace && !aligned(call.workspace, 16)) return PKV_ERR_MISALIGNED;
+    if (int8) {
+        return call.head_dim == 128 ? launch<true, 128>(call, sh) : launch<true, 64>(call, sh);
+    }
+    return call.head_dim == 128 ? launch<false, 128>(call, sh) : launch<false, 64>(call, sh);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_decode_fp16(float *out, const void *query, const void *k_cache,
+                                            const void *v_cache, int num_blocks,
+                                            const int32_t *block_tables, int max_blocks_per_seq,
+                                            const int32_t *context_lens, int max_context_len,
+                                            int num_seqs, int num_heads, int num_kv_heads,
+                                            int head_dim, int block_size, float softmax_scale,
+                                            void *workspace, size_t workspace_bytes,
+                                            int32_t *dev_status, void *stream)
+{
+    const pkv::DecodeCall call{out, query, k_cache, v_cache, nullptr, nullptr, num_blocks,
+                               block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                               num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                               softmax_scale, workspace, workspace_bytes, dev_status, stream};
+    return pkv::decode_entry(call, false);
+}
+
+extern "C" pkv_status pkv_paged_decode_int8(float *out, const void *query, const int8_t *k_codes,
+                                            const int8_t *v_codes, const float *k_scales,
+                                            const float *v_scales, int num_blocks,
+                                            const int32_t *block_tables, int max_blocks_per_seq,
+                                            const int32_t *context_lens, int max_context_len,
+                                            int num_seqs, int num_heads, int num_kv_heads,
+                                            int head_dim, int block_size, float softmax_scale,
+                                            void *workspace, size_t workspace_bytes,
+                                            int32_t *dev_status, void *stream)
+{
+    const pkv::DecodeCall call{out, query, k_codes, v_codes, k_scales, v_scales, num_blocks,
+                               block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                               num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                               softmax_scale, workspace, workspace_bytes, dev_status, stream};
+    return pkv::decode_entry(call, true);
+}
+
+extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                            int head_dim, int max_context_len)
+{
+    pkv::Shape sh;
+    // the block table can hold any context up to max_context_len here
+    const int mbps = (max_context_len + 15) / 16;
+    if (pkv::check_shape(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, mbps,
+                         &sh) != PKV_OK)
+        return 0;
+    return pkv::workspace_bytes_for(sh, head_dim);
+}
+
+extern "C" pkv_status pkv_set_decode_workers(int max_workers)
+{
+    if (max_workers < 0) return PKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(pkv::g_cfg_mu);
+    pkv::g_worker_cap = max_workers;
+    return PKV_OK;
+}

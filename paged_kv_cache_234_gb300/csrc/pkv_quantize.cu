@@ -1,0 +1,133 @@
+// pkv_quantize.cu -- symmetric per-(block, kv head) INT8 quantization of fp16
+// K and V tiles (PagedKV-Fusion README, "Overview" component B and the
+// "Architecture" sequence diagram step "INT8 survivors + scales").
+//
+// One warp per (block, kv head, K|V) tile of 16 x head_dim fp16 values.  The
+// tile is read once with 16-byte loads (coalesced across the warp), max |x|
+// is reduced with warp shuffles, scale = max / 127 with an IEEE fp32
+// division, and every code is the half-even rounding of the IEEE fp32
+// quotient x / scale.  HBM-bound: 2 bytes read and 1 byte written per value,
+// plus 4 bytes of scale per tile.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "pkv_host.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kQuantWarps = 8;
+
+__device__ __forceinline__ int quant_code(float x, float scale)
+{
+    const float y = __fdiv_rn(x, scale);
+    if (isnan(y)) return 0;  // 0/0, inf/inf or a NaN input
+    int c = __float2int_rn(y);
+    c = c > 127 ? 127 : c;
+    c = c < -127 ? -127 : c;
+    return c;
+}
+
+// kChunks: 16-byte chunks of the tile handled by each lane.
+template <int kHeadDim>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    quantize_kernel(const __half *__restrict__ k_in, const __half *__restrict__ v_in,
+                    int8_t *__restrict__ k_out, int8_t *__restrict__ v_out,
+                    float *__restrict__ k_scales, float *__restrict__ v_scales,
+                    const int32_t *__restrict__ block_ids, int64_t tiles_per_pool,
+                    int num_kv_heads, int num_blocks, int32_t *dev_status)
+{
+    constexpr int kTileElems = 16 * kHeadDim;
+    constexpr int kChunks = kTileElems / 8 / 32;  // 16-byte chunks per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+    if (gwarp >= 2 * tiles_per_pool) return;
+    const bool is_v = gwarp >= tiles_per_pool;
+    const int64_t t = is_v ? gwarp - tiles_per_pool : gwarp;
+    const int64_t j = t / num_kv_heads;
+    const int h = static_cast<int>(t % num_kv_heads);
+    const int64_t blk = block_ids ? static_cast<int64_t>(block_ids[j]) : j;
+    if (blk < 0 || blk >= num_blocks) {
+        if (lane == 0 && h == 0 && !is_v && dev_status) atomicOr(dev_status, PKV_DEV_BAD_BLOCK);
+        return;
+    }
+    const int64_t tile = blk * num_kv_heads + h;
+    const uint4 *src = reinterpret_cast<const uint4 *>((is_v ? v_in : k_in) + tile * kTileElems);
+    uint2 *dst = reinterpret_cast<uint2 *>((is_v ? v_out : k_out) + tile * kTileElems);
+
+    uint4 raw[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) raw[c] = __ldcs(src + c * 32 + lane);
+
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        const __half2 *p = reinterpret_cast<const __half2 *>(&raw[c]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(p[e]);
+            amax = fmaxf(amax, fabsf(f.x));  // fmaxf drops a NaN operand
+            amax = fmaxf(amax, fabsf(f.y));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, 127.0f);
+
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        const __half2 *p = reinterpret_cast<const __half2 *>(&raw[c]);
+        uint32_t packed[2];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const float2 f0 = __half22float2(p[2 * w]);
+            const float2 f1 = __half22float2(p[2 * w + 1]);
+            const uint32_t b0 = static_cast<uint32_t>(quant_code(f0.x, scale)) & 0xffu;
+            const uint32_t b1 = static_cast<uint32_t>(quant_code(f0.y, scale)) & 0xffu;
+            const uint32_t b2 = static_cast<uint32_t>(quant_code(f1.x, scale)) & 0xffu;
+            const uint32_t b3 = static_cast<uint32_t>(quant_code(f1.y, scale)) & 0xffu;
+            packed[w] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        }
+        __stcs(dst + c * 32 + lane, make_uint2(packed[0], packed[1]));
+    }
+    if (lane == 0) (is_v ? v_scales : k_scales)[tile] = scale;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16, int8_t *k_codes,
+                                          int8_t *v_codes, float *k_scales, float *v_scales,
+                                          const int32_t *block_ids, int num_ids, int num_blocks,
+                                          int num_kv_heads, int head_dim, int block_size,
+                                          int32_t *dev_status, void *stream)
+{
+    using namespace pkv;
+    if (!k_fp16 || !v_fp16 || !k_codes || !v_codes || !k_scales || !v_scales)
+        return PKV_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || num_kv_heads <= 0 || num_ids < 0 || head_dim <= 0 || block_size <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (block_size != 16 || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(k_fp16, 16) || !aligned(v_fp16, 16) || !aligned(k_codes, 16) ||
+        !aligned(v_codes, 16) || !aligned(k_scales, 4) || !aligned(v_scales, 4) ||
+        (block_ids && !aligned(block_ids, 4)) || (dev_status && !aligned(dev_status, 4)))
+        return PKV_ERR_MISALIGNED;
+    const int64_t count = block_ids ? num_ids : num_blocks;
+    const int64_t tiles = count * num_kv_heads;
+    if (tiles == 0) return PKV_OK;
+    const int64_t warps = 2 * tiles;
+    const int64_t grid = (warps + kQuantWarps - 1) / kQuantWarps;
+    if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 g(static_cast<unsigned>(grid)), b(kQuantWarps * 32);
+    if (head_dim == 128) {
+        quantize_kernel<128><<<g, b, 0, s>>>(
+            static_cast<const __half *>(k_fp16), static_cast<const __half *>(v_fp16), k_codes,
+            v_codes, k_scales, v_scales, block_ids, tiles, num_kv_heads, num_blocks, dev_status);
+    } else {
+        quantize_kernel<64><<<g, b, 0, s>>>(
+            static_cast<const __half *>(k_fp16), static_cast<const __half *>(v_fp16), k_codes,
+            v_codes, k_scales, v_scales, block_ids, tiles, num_kv_heads, num_blocks, dev_status);
+    }
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

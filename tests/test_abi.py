@@ -1,0 +1,129 @@
+"""The C-ABI library builds, loads and exports every declared call; host-side
+argument checks return the documented status codes without touching a GPU.
+
+Nothing here launches a kernel or makes a CUDA call: every case below is
+rejected (or is a no-op) before the library reaches the CUDA runtime.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_234_gb300 as pkv
+from paged_kv_cache_234_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    pkv_build.build()
+    return pkv.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pkv_quantize_blocks", "pkv_paged_decode_fp16", "pkv_paged_decode_int8"):
+        assert required in names
+    assert set(names) == set(pkv.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert pkv.pkv_status_string(code)
+    assert pkv.pkv_status_string(0) == "ok"
+    assert pkv.pkv_status_string(99) == "unknown status"
+
+
+def test_workspace_size_arithmetic(L):
+    # two partial records per worker, min(8, group) heads each, (d + 4) floats
+    # per record; at most 4096 workers and never more than the pages.
+    assert pkv.pkv_decode_workspace_size(64, 32, 8, 128, 2048) == 4096 * 2 * 4 * 132 * 4
+    assert pkv.pkv_decode_workspace_size(2, 8, 2, 64, 37) == (2 * 2 * 3) * 2 * 4 * 68 * 4
+    assert pkv.pkv_decode_workspace_size(8, 8, 8, 128, 512) == 2048 * 2 * 1 * 132 * 4
+    assert pkv.pkv_decode_workspace_size(1, 32, 1, 128, 16) == 4 * 2 * 8 * 132 * 4
+    assert pkv.pkv_decode_workspace_size(4, 8, 3, 128, 16) == 0      # heads not divisible
+    assert pkv.pkv_decode_workspace_size(4, 8, 2, 96, 16) == 0       # unsupported head_dim
+    assert pkv.pkv_decode_workspace_size(0, 8, 2, 64, 0) == 0
+
+
+FAKE = 0x10000  # an aligned, never-dereferenced address
+
+
+def _decode(L, int8=False, **kw):
+    a = dict(out=FAKE, query=FAKE, k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, num_blocks=16,
+             tables=FAKE, mb=4, lens=FAKE, max_ctx=64, n=2, hq=8, hkv=2, d=64, bs=16,
+             scale=0.125, ws=FAKE, ws_bytes=1 << 30, status=None, stream=None)
+    a.update(kw)
+    head = [a["out"], a["query"], a["k"], a["v"]]
+    if int8:
+        head += [a["ks"], a["vs"]]
+    args = head + [a["num_blocks"], a["tables"], a["mb"], a["lens"], a["max_ctx"], a["n"],
+                   a["hq"], a["hkv"], a["d"], a["bs"], a["scale"], a["ws"], a["ws_bytes"],
+                   a["status"], a["stream"]]
+    fn = L.pkv_paged_decode_int8 if int8 else L.pkv_paged_decode_fp16
+    return fn(*args)
+
+
+@pytest.mark.parametrize("int8", [False, True])
+def test_decode_host_validation(L, int8):
+    assert _decode(L, int8, out=None) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, int8, tables=None) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, int8, hq=7) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, int8, n=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, int8, scale=float("nan")) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, int8, d=96) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(L, int8, bs=32) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(L, int8, n=9000) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(L, int8, k=FAKE + 4) == pkv.PKV_ERR_MISALIGNED
+    assert _decode(L, int8, out=FAKE + 8) == pkv.PKV_ERR_MISALIGNED
+    assert _decode(L, int8, ws_bytes=100) == pkv.PKV_ERR_WORKSPACE
+    assert _decode(L, int8, ws=None) == pkv.PKV_ERR_WORKSPACE
+    assert _decode(L, int8, n=0) == pkv.PKV_OK  # nothing to do, nothing launched
+    if int8:
+        assert _decode(L, int8, ks=None) == pkv.PKV_ERR_INVALID_ARG
+        assert _decode(L, int8, vs=FAKE + 2) == pkv.PKV_ERR_MISALIGNED
+
+
+def test_quantize_host_validation(L):
+    def q(**kw):
+        a = dict(k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE, ids=None, nids=0,
+                 nb=16, hkv=2, d=64, bs=16, status=None, stream=None)
+        a.update(kw)
+        return L.pkv_quantize_blocks(a["k"], a["v"], a["kc"], a["vc"], a["ks"], a["vs"],
+                                     a["ids"], a["nids"], a["nb"], a["hkv"], a["d"], a["bs"],
+                                     a["status"], a["stream"])
+    assert q(k=None) == pkv.PKV_ERR_INVALID_ARG
+    assert q(nb=0) == pkv.PKV_ERR_INVALID_ARG
+    assert q(nids=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert q(d=96) == pkv.PKV_ERR_UNSUPPORTED
+    assert q(bs=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert q(kc=FAKE + 1) == pkv.PKV_ERR_MISALIGNED
+    assert q(ids=FAKE, nids=0) == pkv.PKV_OK  # empty id list: nothing launched
+
+
+def test_set_decode_workers_rejects_negative(L):
+    assert L.pkv_set_decode_workers(-1) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_set_decode_workers(0) == pkv.PKV_OK
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_cache_234_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "pkv_oracle" not in text, f
