@@ -214,6 +214,39 @@ def cpu_baseline(w, seconds=10.0):
                       f"({dt:.1f} s)"}
 
 
+def run_profile(args):
+    """Decode calls of one variant on the benchmark batch placed in a smaller
+    pool (same bytes per call), for ncu captures that must stay small."""
+    import torch
+    import paged_kv_cache_234_gb300 as pkv
+    from paged_kv_cache_234_gb300 import build as pkv_build
+    pkv_build.build()
+    w = W.build(CONFIG + "_pool16k", num_heads=32, num_kv_heads=8, head_dim=128,
+                num_blocks=16384, context_lens=[2048] * 64, seed=1005)
+    n, hq, d = w.query.shape
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    kf, vf = dev(w.k_pool), dev(w.v_pool)
+    q, bt, cl = dev(w.query), dev(w.block_tables), dev(w.context_lens)
+    out = torch.empty((n, hq, d), dtype=torch.float32, device="cuda")
+    ws_t = pkv.decode_workspace(n, hq, w.num_kv_heads, d, w.max_context_len)
+    if args.profile == "int8":
+        kc = torch.zeros(w.k_pool.shape, dtype=torch.int8, device="cuda")
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros(w.k_pool.shape[:2], dtype=torch.float32, device="cuda")
+        vs = torch.zeros_like(ks)
+        pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, dev(w.used_block_ids))
+        del kf, vf
+        call = lambda: pkv.pkv_paged_decode_int8(out, q, kc, vc, ks, vs, bt, cl,
+                                                 w.max_context_len, w.softmax_scale, ws_t)
+    else:
+        call = lambda: pkv.pkv_paged_decode_fp16(out, q, kf, vf, bt, cl, w.max_context_len,
+                                                 w.softmax_scale, ws_t)
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    print(f"profile run: {args.profile} decode x{args.warmup + args.steps}", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -222,10 +255,16 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", choices=["int8", "fp16"],
+                    help="profiling run: the same batch over a 16384-block pool, only "
+                         "warm-up + timed decode calls of one variant, no report line")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+        return
+    if args.profile:
+        run_profile(args)
         return
 
     import torch
@@ -285,7 +324,7 @@ def main():
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler = ClockSampler(local)
     sampler.start()
     if pg:
@@ -295,31 +334,34 @@ def main():
         flush.zero_()
         ev[i][0].record(stream)
         step_int8()
-        ev[i][1].record(stream)
         decode_int8()
-        ev[i][2].record(stream)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
     clocks = sampler.stop()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     total_ms = sum(step_ms)
     if pg:
         t = torch.tensor([total_ms], device="cuda")
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         total_ms = float(t.item())
 
-    # fp16 decode of the same batch (reported as a variant)
-    Kf = min(K, 500)
-    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kf)]
-    for i in range(Kf):
-        flush.zero_()
-        evf[i][0].record(stream)
-        decode_fp16()
-        evf[i][1].record(stream)
-    torch.cuda.synchronize()
-    f16_ms = [e[0].elapsed_time(e[1]) for e in evf]
+    # each decode variant alone (the dominant kernel, for the roofline)
+    def timed(fn, reps):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+        for i in range(reps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in evs]
+
+    Kd = min(K, 500)
+    dec_ms = timed(decode_int8, Kd)
+    f16_ms = timed(decode_fp16, Kd)
+    q_ms = timed(step_int8, Kd)
 
     # end to end through the public API with host buffers: per step the
     # query, block tables, context lengths and tail ids go host -> device and
@@ -387,6 +429,9 @@ def main():
                             "bytes": f16_b},
             "decode_int8": {"p50_us": 1e3 * statistics.median(dec_ms), "GB/s": achieved,
                             "bytes": dec_b},
+            "quantize_tail_blocks": {"p50_us": 1e3 * statistics.median(q_ms),
+                                     "tiles": 2 * ntiles,
+                                     "bytes": quantize_bytes(ntiles, d)},
         },
         "e2e": {"value": step_b * Ke / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},

@@ -13,30 +13,35 @@
 // query heads of that kv head); its pages are the sequence's 16-token
 // blocks.  All items' pages form one stream of T pages, and every warp of a
 // persistent grid (one worker per resident warp) streams one contiguous,
-// equal share of it.  A worker's share is therefore a run of "pieces": at
-// most one partial item at each end and whole items in between.  Whole items
-// are finished in place; partial pieces leave (running max, running sum,
+// equal share of it, so every SM moves the same number of bytes whatever the
+// mix of context lengths.  A worker's share is a run of "pieces": at most one
+// partial item at each end and whole items in between.  Whole items are
+// finished in place; a partial piece leaves (running max, running sum,
 // unnormalised accumulator) in the workspace, and the split-context reduce
-// kernel merges the pieces of each split item.  This gives every SM the same
-// number of bytes whatever the mix of context lengths.
+// kernel, launched as a programmatic dependent of the decode grid, merges the
+// pieces of every split item.
 //
 // Per worker (warp), pages flow through a private ring of S shared-memory
-// stages.  Lane 0 issues TMA tile loads (16 rows x head_dim, 128- or 64-byte
-// swizzled) for the K and V tiles of a page, plus 4-byte cp.async copies of
-// the two INT8 scales, all completing on the stage's mbarrier; the ring
-// keeps S pages in flight while the warp computes on the oldest one.
+// stages of one or two pages each.  Lane 0 issues TMA tile loads (16 rows x
+// head_dim, 128- or 64-byte swizzled) for the K and V tiles of the stage's
+// pages, plus 4-byte cp.async copies of the INT8 scales, all completing on
+// the stage's mbarrier; the ring keeps the next stages in flight while the
+// warp computes on the oldest one.
 //
 // Per page, the GQA group's query heads (up to 8) share one read of K and V:
 //   S^T[16 tok][8 heads] = K_page[16 x d] . Q^T      (m16n8k16, f16 -> f32)
-//   online softmax in base 2 (scores pre-multiplied by scale*log2 e)
+//   online softmax in base 2, one update per stage
 //   O^T[d][8 heads]     += V_page^T[d x 16] . P^T    (m16n8k16, f16 -> f32)
-// INT8 codes are widened to f16 exactly (byte-permute into 1024 + code + 128,
-// subtract 1152); the K scale multiplies the scores and the V scale the
-// probabilities, so dequantisation costs one multiply per score.
+// INT8 codes are widened to f16 exactly by byte permutes: a code c placed
+// under the exponent byte 0x64 reads as 1152 + c.  For K the constant 1152
+// is left in and removed from the scores as 1152 * sum(q); for V it is
+// subtracted before the product.  The K scale multiplies the scores and the
+// V scale the probabilities.
 #include <cuda_fp16.h>
 #include <stdint.h>
 
 #include <mutex>
+#include <utility>
 
 #include "pkv_host.cuh"
 #include "pkv_ptx.cuh"
@@ -62,7 +67,9 @@ struct DecodeArgs {
     const int32_t *context_lens;
     const float *k_scales;
     const float *v_scales;
-    float *partials;  // [num_workers * 2][rec_heads][head_dim + 4]
+    float *partials;     // [num_workers * 2][rec_heads][head_dim + 4]
+    int4 *splits;        // [num_workers][2]: the split item whose first piece
+                         // the worker holds, if any (see SplitDesc)
     int32_t *dev_status;
     int num_seqs, num_heads, num_kv_heads;
     int group;           // query heads per kv head
@@ -76,20 +83,65 @@ struct DecodeArgs {
     float scale_log2;    // softmax_scale * log2(e)
 };
 
+// Pipeline shape per variant: pages per stage, stages per warp, CTAs (of
+// four warps) per SM.  Shared memory per CTA is 4 * stages * pages * (K + V
+// tile) bytes; the register budget follows from the CTA count.
+#ifndef PKV_F16_D128_PPS
+#define PKV_F16_D128_PPS 1
+#endif
+#ifndef PKV_F16_D128_STAGES
+#define PKV_F16_D128_STAGES 2
+#endif
+#ifndef PKV_F16_D128_CTAS
+#define PKV_F16_D128_CTAS 3
+#endif
+#ifndef PKV_I8_D128_PPS
+#define PKV_I8_D128_PPS 2
+#endif
+#ifndef PKV_I8_D128_STAGES
+#define PKV_I8_D128_STAGES 2
+#endif
+#ifndef PKV_I8_D128_CTAS
+#define PKV_I8_D128_CTAS 3
+#endif
+
+template <int kPPS_, int kStages_, int kMinCtas_>
+struct Tune {
+    static constexpr int kPPS = kPPS_;
+    static constexpr int kStages = kStages_;
+    static constexpr int kMinCtas = kMinCtas_;
+};
+
+template <bool kInt8, int kD>
+struct TuneOf;
+template <>
+struct TuneOf<false, 128> : Tune<PKV_F16_D128_PPS, PKV_F16_D128_STAGES, PKV_F16_D128_CTAS> {};
+template <>
+struct TuneOf<true, 128> : Tune<PKV_I8_D128_PPS, PKV_I8_D128_STAGES, PKV_I8_D128_CTAS> {};
+template <>
+struct TuneOf<false, 64> : Tune<1, 3, 4> {};
+template <>
+struct TuneOf<true, 64> : Tune<2, 3, 4> {};
+
 template <bool kInt8, int kD>
 struct Cfg {
     static constexpr int kElem = kInt8 ? 1 : 2;
     static constexpr int kRowBytes = kD * kElem;                 // 256 / 128 / 64
     static constexpr int kTileBytes = kPage * kRowBytes;         // one (block, kv head) tile
-    static constexpr int kStageBytes = 2 * kTileBytes;           // K tile + V tile
+    static constexpr int kPageBytes = 2 * kTileBytes;            // K tile + V tile
+    static constexpr int kPPS = TuneOf<kInt8, kD>::kPPS;         // pages per stage
+    static constexpr int kStageBytes = kPPS * kPageBytes;
     static constexpr int kBoxInner = kRowBytes > 128 ? 128 / kElem : kD;  // elements
     static constexpr int kBoxes = kD / kBoxInner;
     static constexpr int kBoxBytes = kPage * kBoxInner * kElem;
     static constexpr int kSwizzle = kRowBytes >= 128 ? 128 : 64;
-    static constexpr int kStages = kStageBytes >= 8192 ? 3 : kStageBytes >= 4096 ? 4 : 6;
+    static constexpr int kStages = TuneOf<kInt8, kD>::kStages;
+    static constexpr int kMinCtas = TuneOf<kInt8, kD>::kMinCtas;
+    static_assert(kPPS == 1 || kPPS == 2, "one or two pages per stage");
+    static constexpr int kHdrBytes = 32;  // per stage: bad[2], k scale[2], v scale[2]
     static constexpr int kStageRegion = kWarps * kStages * kStageBytes;
-    static constexpr int kHdrOffset = kStageRegion;                         // 16 B per stage
-    static constexpr int kBarOffset = kHdrOffset + kWarps * kStages * 16;   // 8 B per stage
+    static constexpr int kHdrOffset = kStageRegion;
+    static constexpr int kBarOffset = kHdrOffset + kWarps * kStages * kHdrBytes;
     static constexpr int kTabOffset = kBarOffset + kWarps * kStages * 8;
     static size_t smem_bytes(int num_seqs)
     {
@@ -175,9 +227,18 @@ struct PageCursor {
         page = static_cast<int>(r % npages);
     }
 
-    __device__ void next(const DecodeArgs &p, const int32_t *prefix)
+    // pages of the next stage: up to kPPS, never past the item's end or `left`
+    __device__ __forceinline__ int unit(int pps, int left) const
     {
-        if (++page < npages) return;
+        int u = npages - page;
+        u = u < pps ? u : pps;
+        return u < left ? u : left;
+    }
+
+    __device__ void advance(const DecodeArgs &p, const int32_t *prefix, int k)
+    {
+        page += k;
+        if (page < npages) return;
         page = 0;
         if (++item < p.items_per_seq) return;
         item = 0;
@@ -194,12 +255,18 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// exact int8 -> f16 pair: bytes (c + 128) under exponent 0x64 give 1024 + c + 128
-__device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t biased_word, uint32_t sel)
+// two int8 codes (bytes picked by sel from a word already XOR-ed with 0x80)
+// as an f16 pair 1152 + c, exact
+__device__ __forceinline__ uint32_t i8pair_biased(uint32_t xw, uint32_t sel)
 {
-    const uint32_t h = ptx::prmt(biased_word, 0x64646464u, sel);
+    return ptx::prmt(xw, 0x64646464u, sel);
+}
+
+// the same pair with the bias removed: exactly c
+__device__ __forceinline__ uint32_t i8pair_exact(uint32_t xw, uint32_t sel)
+{
     uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(i8pair_biased(xw, sel)), "r"(0x64806480u));
     return r;
 }
 
@@ -209,13 +276,131 @@ __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t total, int worke
     return ((x + 1) * workers - 1) / total;
 }
 
+// Per worker: the item split across workers whose first page lies in this
+// worker's range, if any.  Word 0: bit 0 valid, bit 1 the record slot of
+// this worker, bit 2 "every worker has pages"; then the last worker holding
+// a piece of the item, the sequence, the item, and the stream length.
+__device__ __forceinline__ void write_split(const DecodeArgs &p, int w, bool valid, int slot,
+                                            int64_t last_worker, int seq, int item, int64_t total)
+{
+    const int flags = (valid ? 1 : 0) | (slot << 1) | (total >= p.num_workers ? 4 : 0);
+    p.splits[2 * w] = make_int4(flags, static_cast<int>(last_worker), seq, item);
+    p.splits[2 * w + 1] = make_int4(static_cast<int>(total), 0, 0, 0);
+}
+
+// S^T fragment (rows: tokens g, g+8; cols: heads 2c, 2c+1) of one page.
 template <bool kInt8, int kD>
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD / 16][2],
+                                            int lane, float (&s)[4])
+{
+    using C = Cfg<kInt8, kD>;
+    constexpr int KS = kD / 16;
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (!kInt8) {
+        const int lt = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int lch = lane >> 4;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a0, a1, a2, a3;
+            ptx::ldsm_x4(kt + swz<C::kRowBytes>(lt, 2 * ks + lch), a0, a1, a2, a3);
+            if (ks & 1)
+                ptx::mma_16816(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            else
+                ptx::mma_16816(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        }
+    } else {
+        // lane (g, c): rows g and g+8, bytes [DG*c, DG*c + DG), DG = kD/4; the
+        // head_dim order matches the query fragments
+        const int g = lane >> 2, c = lane & 3;
+        constexpr int CH = kD / 64;  // 16-byte chunks per row per lane
+        uint32_t kw[2][4 * CH];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                const uint4 v = ptx::lds128(kt + swz<C::kRowBytes>(g + 8 * r, CH * c + j));
+                kw[r][4 * j + 0] = v.x ^ 0x80808080u;
+                kw[r][4 * j + 1] = v.y ^ 0x80808080u;
+                kw[r][4 * j + 2] = v.z ^ 0x80808080u;
+                kw[r][4 * j + 3] = v.w ^ 0x80808080u;
+            }
+        }
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const uint32_t a0 = i8pair_biased(kw[0][ks], 0x4140u);
+            const uint32_t a2 = i8pair_biased(kw[0][ks], 0x4342u);
+            const uint32_t a1 = i8pair_biased(kw[1][ks], 0x4140u);
+            const uint32_t a3 = i8pair_biased(kw[1][ks], 0x4342u);
+            if (ks & 1)
+                ptx::mma_16816(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            else
+                ptx::mma_16816(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = sa[i] + sb[i];
+}
+
+// O^T += V_page^T . P^T for one page; tokens >= ntok contribute nothing.
+template <bool kInt8, int kD>
+__device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1, int ntok,
+                                        int lane, float (&o)[kD / 16][4])
+{
+    using C = Cfg<kInt8, kD>;
+    constexpr int KS = kD / 16;
+    const int g = lane >> 2, c = lane & 3;
+    if constexpr (!kInt8) {
+        const int lt = (lane & 7) + 8 * (lane >> 4);
+        const int lch = (lane >> 3) & 1;
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (ntok < kPage) {  // zero V rows of tokens past the end (they may hold NaN)
+            mlo = (2 * c < ntok ? 0x0000ffffu : 0u) | (2 * c + 1 < ntok ? 0xffff0000u : 0u);
+            mhi = (2 * c + 8 < ntok ? 0x0000ffffu : 0u) | (2 * c + 9 < ntok ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+            uint32_t a0, a1, a2, a3;
+            ptx::ldsm_x4_t(vt + swz<C::kRowBytes>(lt, 2 * i + lch), a0, a1, a2, a3);
+            ptx::mma_16816(o[i], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+        }
+    } else {
+        // lane (g, c): tokens 2c, 2c+1, 2c+8, 2c+9; bytes [DG*g, DG*g + DG), DG = kD/8
+        constexpr int NW = kD / 32;  // words per token per lane
+        uint32_t vw[4][NW];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = 2 * c + (r & 1) + 8 * (r >> 1);
+            if constexpr (kD == 128) {
+                const uint4 v = ptx::lds128(vt + swz<C::kRowBytes>(t, g));
+                vw[r][0] = v.x ^ 0x80808080u;
+                vw[r][1] = v.y ^ 0x80808080u;
+                vw[r][2] = v.z ^ 0x80808080u;
+                vw[r][3] = v.w ^ 0x80808080u;
+            } else {
+                const uint2 v = ptx::lds64(vt + swz<C::kRowBytes>(t, g >> 1) + (g & 1) * 8);
+                vw[r][0] = v.x ^ 0x80808080u;
+                vw[r][1] = v.y ^ 0x80808080u;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+            const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+            const uint32_t il01 = ptx::prmt(vw[0][i >> 1], vw[1][i >> 1], sel);
+            const uint32_t il23 = ptx::prmt(vw[2][i >> 1], vw[3][i >> 1], sel);
+            ptx::mma_16816(o[i], i8pair_exact(il01, 0x4140u), i8pair_exact(il01, 0x4342u),
+                           i8pair_exact(il23, 0x4140u), i8pair_exact(il23, 0x4342u), pb0, pb1);
+        }
+    }
+}
+
+template <bool kInt8, int kD>
+__global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
     decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv)
 {
     using C = Cfg<kInt8, kD>;
     constexpr int S = C::kStages;
+    constexpr int PPS = C::kPPS;
     constexpr int KS = kD / 16;  // mma k-steps over head_dim, also m-tiles of O^T
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -229,6 +414,12 @@ __global__ void __launch_bounds__(kThreads)
         ptx::prefetch_tmap(&tmk);
         ptx::prefetch_tmap(&tmv);
     }
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: wait until its writes are visible before reading any input.
+    ptx::griddep_wait();
+    // The next kernel on the stream may begin its own launch now; it waits
+    // for this grid's completion before reading anything this grid writes.
+    ptx::griddep_launch_dependents();
     build_page_tables(p, prefix, ctxs);
     const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
 
@@ -242,16 +433,17 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     const int w = blockIdx.x * kWarps + warp;
-    if (w >= p.num_workers || total == 0) return;
+    if (w >= p.num_workers) return;
+    if (lane == 0) write_split(p, w, false, 0, 0, 0, 0, total);  // no split item yet
+    if (total == 0) return;
     const int64_t a = w * total / p.num_workers;
     const int64_t b = (w + 1) * total / p.num_workers;
     if (a >= b) return;
-    const int64_t n = b - a;
+    const int n = static_cast<int>(b - a);  // pages of this worker
 
     const uint32_t stage0 = ptx::smem_addr(smem) + warp * S * C::kStageBytes;
-    const uint32_t hdr0 = ptx::smem_addr(smem + C::kHdrOffset) + warp * S * 16;
-    int32_t *hdr_bad = reinterpret_cast<int32_t *>(smem + C::kHdrOffset) + warp * S * 4;
-    const float *hdr_f = reinterpret_cast<const float *>(hdr_bad);
+    uint8_t *hdr_base = smem + C::kHdrOffset + warp * S * C::kHdrBytes;
+    const uint32_t hdr0 = ptx::smem_addr(hdr_base);
     const uint32_t bar0 = ptx::smem_addr(smem + C::kBarOffset) + warp * S * 8;
     if (lane == 0) {
         for (int s = 0; s < S; ++s) ptx::mbar_init(bar0 + 8 * s, kInt8 ? 2 : 1);
@@ -261,69 +453,99 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t policy = ptx::policy_evict_first();
     const int64_t mb = p.max_blocks_per_seq;
 
-    // Lane 0: start the copies of one page into stage `slot`.
-    auto issue = [&](int slot, int32_t blk, int kvh) {
+    // Lane 0: start the copies of the `cnt` pages of one stage; blk[u] are
+    // their block ids, kvh the kv head of the item.
+    auto issue = [&](int slot, int cnt, const int32_t (&blk)[PPS], int kvh) {
         const uint32_t bar = bar0 + 8 * slot;
-        if (blk < 0 || blk >= p.num_blocks) {
-            hdr_bad[slot * 4] = 1;
-            if (p.dev_status) atomicOr(p.dev_status, PKV_DEV_BAD_BLOCK);
-            ptx::mbar_arrive(bar);
-            if (kInt8) ptx::mbar_arrive(bar);
-            return;
-        }
-        hdr_bad[slot * 4] = 0;
-        ptx::mbar_arrive_expect_tx(bar, C::kStageBytes);
-        const int row = (blk * p.num_kv_heads + kvh) * kPage;
-        const uint32_t kdst = stage0 + slot * C::kStageBytes;
+        int32_t *hb = reinterpret_cast<int32_t *>(hdr_base + slot * C::kHdrBytes);
+        uint32_t bytes = 0;
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-            ptx::tma_load_2d(kdst + bx * C::kBoxBytes, &tmk, bx * C::kBoxInner, row, bar, policy);
-            ptx::tma_load_2d(kdst + C::kTileBytes + bx * C::kBoxBytes, &tmv, bx * C::kBoxInner, row,
-                             bar, policy);
+        for (int u = 0; u < PPS; ++u) {
+            const bool ok = u < cnt && blk[u] >= 0 && blk[u] < p.num_blocks;
+            hb[u] = ok ? 0 : 1;
+            if (u < cnt && !ok && p.dev_status) atomicOr(p.dev_status, PKV_DEV_BAD_BLOCK);
+            bytes += ok ? C::kPageBytes : 0;
         }
-        if constexpr (kInt8) {
-            const int64_t si = static_cast<int64_t>(blk) * p.num_kv_heads + kvh;
-            ptx::cp_async_4(hdr0 + slot * 16 + 4, p.k_scales + si);
-            ptx::cp_async_4(hdr0 + slot * 16 + 8, p.v_scales + si);
-            ptx::cp_async_arrive_noinc(bar);
+        ptx::mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+        for (int u = 0; u < PPS; ++u) {
+            if (hb[u]) continue;
+            const int row = (blk[u] * p.num_kv_heads + kvh) * kPage;
+            const uint32_t kdst = stage0 + slot * C::kStageBytes + u * C::kPageBytes;
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx) {
+                ptx::tma_load_2d(kdst + bx * C::kBoxBytes, &tmk, bx * C::kBoxInner, row, bar,
+                                 policy);
+                ptx::tma_load_2d(kdst + C::kTileBytes + bx * C::kBoxBytes, &tmv,
+                                 bx * C::kBoxInner, row, bar, policy);
+            }
+            if constexpr (kInt8) {
+                const int64_t si = static_cast<int64_t>(blk[u]) * p.num_kv_heads + kvh;
+                ptx::cp_async_4(hdr0 + slot * C::kHdrBytes + 8 + 4 * u, p.k_scales + si);
+                ptx::cp_async_4(hdr0 + slot * C::kHdrBytes + 16 + 4 * u, p.v_scales + si);
+            }
         }
+        if constexpr (kInt8) ptx::cp_async_arrive_noinc(bar);
     };
 
-    // ---- prologue: block ids of the first pages, one lane each, then issue
+    // ---- prologue: block ids of the first stages (one lane per page), issue
     PageCursor ci;
     ci.seek(p, prefix, a);
     PageCursor cc = ci;
-    const int pro = static_cast<int>(n < S ? n : S);
+    int ipos = 0;          // pages issued so far
+    uint32_t issued = 0;   // stages issued so far
     {
+        // lane j*PPS + u holds page u of stage j
         PageCursor cj = ci;
-        for (int j = 0; j < lane && j < pro - 1; ++j) cj.next(p, prefix);
-        const int32_t myblk =
-            lane < pro ? __ldg(p.block_tables + cj.seq * mb + cj.page) : 0;
-        const int mykvh = cj.item / p.qgroups;
-        for (int j = 0; j < pro; ++j) {
-            const int32_t blk = __shfl_sync(0xffffffffu, myblk, j);
-            const int kvh = __shfl_sync(0xffffffffu, mykvh, j);
-            if (lane == 0) issue(j, blk, kvh);
+        int pos = 0;
+        const int my_stage = lane / PPS, my_u = lane % PPS;
+        int32_t myblk = 0;
+        int mykvh = 0, mycnt = 0;
+        for (int j = 0; j < S && pos < n; ++j) {
+            const int cnt = cj.unit(PPS, n - pos);
+            if (j == my_stage) {
+                mycnt = cnt;
+                mykvh = cj.item / p.qgroups;
+                if (my_u < cnt) myblk = __ldg(p.block_tables + cj.seq * mb + cj.page + my_u);
+            }
+            cj.advance(p, prefix, cnt);
+            pos += cnt;
         }
-        for (int j = 0; j < pro; ++j) ci.next(p, prefix);
+        for (int j = 0; j < S && ipos < n; ++j) {
+            const int cnt = __shfl_sync(0xffffffffu, mycnt, j * PPS);
+            const int kvh = __shfl_sync(0xffffffffu, mykvh, j * PPS);
+            int32_t blk[PPS];
+#pragma unroll
+            for (int u = 0; u < PPS; ++u) blk[u] = __shfl_sync(0xffffffffu, myblk, j * PPS + u);
+            if (lane == 0) issue(j, cnt, blk, kvh);
+            ci.advance(p, prefix, cnt);
+            ipos += cnt;
+            ++issued;
+        }
     }
-    int32_t nblk = 0;  // lane 0: block id of the next page to issue
-    if (lane == 0 && pro < n) nblk = __ldg(p.block_tables + ci.seq * mb + ci.page);
+    // lanes u < PPS: block id of page u of the next stage to issue
+    int32_t nblk = 0;
+    if (ipos < n && lane < ci.unit(PPS, n - ipos))
+        nblk = __ldg(p.block_tables + ci.seq * mb + ci.page + lane);
 
     // ---- per-piece state
     float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 units), heads 2c and 2c+1
     float l0 = 0.f, l1 = 0.f;              // lane-partial running sums
     float o[KS][4];                        // O^T accumulators (see the output mapping)
     uint32_t qf[KS][2];                    // Q^T B-fragments
+    float qb0 = 0.f, qb1 = 0.f;            // INT8: 1152 * sum(q) of heads 2c, 2c+1
     bool piece_bad = false;
     bool piece_has_a = true;
     int piece_first_page = 0;
+    int piece_pages = 0;
 
-    for (int64_t k = 0; k < n; ++k) {
+    int pos = 0;
+    for (uint32_t k = 0; pos < n; ++k) {
         const int slot = static_cast<int>(k % S);
-        const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
-        const bool first = (k == 0) || (cc.page == 0);
-        const bool last = (k == n - 1) || (cc.page == cc.npages - 1);
+        const uint32_t parity = (k / S) & 1u;
+        const int cnt = cc.unit(PPS, n - pos);
+        const bool first = pos == 0 || cc.page == 0;
+        const bool last = pos + cnt == n || cc.page + cnt == cc.npages;
         const int kvh = cc.item / p.qgroups;
         const int qg = cc.item - kvh * p.qgroups;
         const int h0 = kvh * p.group + qg * kItemHeads;
@@ -331,7 +553,8 @@ __global__ void __launch_bounds__(kThreads)
 
         if (first) {
             // query fragments of the item's heads; heads past gh are zero
-            const __half *qrow = p.query + (static_cast<int64_t>(cc.seq) * p.num_heads + h0 + g) * kD;
+            const __half *qrow =
+                p.query + (static_cast<int64_t>(cc.seq) * p.num_heads + h0 + g) * kD;
             const bool live = g < gh;
             if constexpr (kInt8) {
                 // lane (g, c) holds q[g][DG*c .. DG*c + DG), DG = kD / 4
@@ -342,11 +565,21 @@ __global__ void __launch_bounds__(kThreads)
                     qv[j] = live ? __ldg(reinterpret_cast<const uint4 *>(qrow + DG * c) + j)
                                  : make_uint4(0, 0, 0, 0);
                 const uint32_t *qw = reinterpret_cast<const uint32_t *>(qv);
+                float qs = 0.f;
 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
                     qf[s][0] = qw[2 * s];
                     qf[s][1] = qw[2 * s + 1];
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&qw[2 * s]));
+                    const float2 f1 =
+                        __half22float2(*reinterpret_cast<const __half2 *>(&qw[2 * s + 1]));
+                    qs += (f0.x + f0.y) + (f1.x + f1.y);
                 }
+                // sum over the head's four lanes, then fetch heads 2c and 2c+1
+                qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+                qb0 = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c);
+                qb1 = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
             } else {
                 const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
 #pragma unroll
@@ -360,85 +593,72 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             piece_bad = false;
-            piece_has_a = (k == 0);
+            piece_has_a = pos == 0;
             piece_first_page = cc.page;
+            piece_pages = 0;
         }
+        piece_pages += cnt;
 
         // every lane waits (acquire); the outcome is made warp-uniform
         const bool landed = ptx::mbar_wait_bounded(bar0 + 8 * slot, parity, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, landed)) {
-            // The copy never landed: report, let the other copies of this
-            // worker land (bounded), and stop this worker.
+            // The copy never landed: report, let this worker's other copies
+            // land (bounded), and stop this worker.
             if (lane == 0 && p.dev_status) atomicOr(p.dev_status, PKV_DEV_TIMEOUT);
-            for (int64_t r = k + 1; r < n && r < k + S; ++r)
-                ptx::mbar_wait_bounded(bar0 + 8 * static_cast<int>(r % S),
-                                       static_cast<uint32_t>((r / S) & 1), kWaitLimitNs);
+            for (uint32_t r = k + 1; r < issued; ++r)
+                ptx::mbar_wait_bounded(bar0 + 8 * (r % S), (r / S) & 1u, kWaitLimitNs);
             return;
         }
 
-        if (hdr_bad[slot * 4]) {
-            piece_bad = true;
-        } else {
-            const int ntok = min(kPage, ctxs[cc.seq] - cc.page * kPage);
-            const uint32_t kt = stage0 + slot * C::kStageBytes;
-            const uint32_t vt = kt + C::kTileBytes;
-            float sk = 1.f, sv = 1.f;
-            if constexpr (kInt8) {
-                sk = hdr_f[slot * 4 + 1];
-                sv = hdr_f[slot * 4 + 2];
-            }
-
-            // ---- S^T = K_page . Q^T   (rows: tokens, cols: heads)
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (!kInt8) {
-                const int lt = (lane & 7) + 8 * ((lane >> 3) & 1);
-                const int lch = lane >> 4;
+        const int32_t *hb = reinterpret_cast<const int32_t *>(hdr_base + slot * C::kHdrBytes);
+        const float *hf = reinterpret_cast<const float *>(hb);
+        bool good[PPS];
+        bool any_good = false;
 #pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    uint32_t a0, a1, a2, a3;
-                    ptx::ldsm_x4(kt + swz<C::kRowBytes>(lt, 2 * s + lch), a0, a1, a2, a3);
-                    if (s & 1)
-                        ptx::mma_16816(sb, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-                    else
-                        ptx::mma_16816(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-                }
-            } else {
-                // lane (g, c): rows g and g+8, bytes [DG*c, DG*c + DG) with DG = kD/4
-                constexpr int CH = kD / 64;  // 16-byte chunks per row per lane
-                uint32_t kw[2][4 * CH];
+        for (int u = 0; u < PPS; ++u) {
+            good[u] = u < cnt && hb[u] == 0;
+            piece_bad |= u < cnt && !good[u];
+            any_good |= good[u];
+        }
+        if (any_good) {
+            const uint32_t st = stage0 + slot * C::kStageBytes;
+            const int ctx = ctxs[cc.seq];
+            // ---- scores of the stage's pages, base-2 logits
+            float x[PPS][4];
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-#pragma unroll
-                    for (int j = 0; j < CH; ++j) {
-                        const uint4 v = ptx::lds128(kt + swz<C::kRowBytes>(g + 8 * r, CH * c + j));
-                        kw[r][4 * j + 0] = v.x ^ 0x80808080u;
-                        kw[r][4 * j + 1] = v.y ^ 0x80808080u;
-                        kw[r][4 * j + 2] = v.z ^ 0x80808080u;
-                        kw[r][4 * j + 3] = v.w ^ 0x80808080u;
+            for (int u = 0; u < PPS; ++u) {
+                if (good[u]) {
+                    float sc[4];
+                    page_scores<kInt8, kD>(st + u * C::kPageBytes, qf, lane, sc);
+                    float sl = p.scale_log2;
+                    if constexpr (kInt8) {
+                        sl *= hf[2 + u];
+                        x[u][0] = (sc[0] - qb0) * sl;
+                        x[u][1] = (sc[1] - qb1) * sl;
+                        x[u][2] = (sc[2] - qb0) * sl;
+                        x[u][3] = (sc[3] - qb1) * sl;
+                    } else {
+                        x[u][0] = sc[0] * sl;
+                        x[u][1] = sc[1] * sl;
+                        x[u][2] = sc[2] * sl;
+                        x[u][3] = sc[3] * sl;
                     }
+                    const int ntok = ctx - (cc.page + u) * kPage;
+                    if (ntok < kPage) {
+                        if (g >= ntok) x[u][0] = x[u][1] = -INFINITY;
+                        if (g + 8 >= ntok) x[u][2] = x[u][3] = -INFINITY;
+                    }
+                } else {
+                    x[u][0] = x[u][1] = x[u][2] = x[u][3] = -INFINITY;
                 }
+            }
+            // ---- online softmax, one update for the whole stage
+            float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    const uint32_t a0 = i8pair_to_h2(kw[0][s], 0x4140u);
-                    const uint32_t a2 = i8pair_to_h2(kw[0][s], 0x4342u);
-                    const uint32_t a1 = i8pair_to_h2(kw[1][s], 0x4140u);
-                    const uint32_t a3 = i8pair_to_h2(kw[1][s], 0x4342u);
-                    if (s & 1)
-                        ptx::mma_16816(sb, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-                    else
-                        ptx::mma_16816(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-                }
+            for (int u = 1; u < PPS; ++u) {
+                mx0 = fmaxf(mx0, fmaxf(x[u][0], x[u][2]));
+                mx1 = fmaxf(mx1, fmaxf(x[u][1], x[u][3]));
             }
-
-            // ---- online softmax (base 2) over this page's tokens
-            const float sl = p.scale_log2 * sk;
-            float x0 = (sa[0] + sb[0]) * sl, x1 = (sa[1] + sb[1]) * sl;  // token g
-            float x2 = (sa[2] + sb[2]) * sl, x3 = (sa[3] + sb[3]) * sl;  // token g+8
-            if (ntok < kPage) {
-                if (g >= ntok) x0 = x1 = -INFINITY;
-                if (g + 8 >= ntok) x2 = x3 = -INFINITY;
-            }
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -446,12 +666,21 @@ __global__ void __launch_bounds__(kThreads)
             }
             const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
             const float al0 = ptx::ex2(m0 - mn0), al1 = ptx::ex2(m1 - mn1);
-            const float p0 = ptx::ex2(x0 - mn0), p1 = ptx::ex2(x1 - mn1);
-            const float p2 = ptx::ex2(x2 - mn0), p3 = ptx::ex2(x3 - mn1);
-            l0 = l0 * al0 + (p0 + p2);
-            l1 = l1 * al1 + (p1 + p3);
             m0 = mn0;
             m1 = mn1;
+            float pr[PPS][4];
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < PPS; ++u) {
+                pr[u][0] = ptx::ex2(x[u][0] - mn0);
+                pr[u][1] = ptx::ex2(x[u][1] - mn1);
+                pr[u][2] = ptx::ex2(x[u][2] - mn0);
+                pr[u][3] = ptx::ex2(x[u][3] - mn1);
+                ps0 += pr[u][0] + pr[u][2];
+                ps1 += pr[u][1] + pr[u][3];
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
             if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
                 for (int i = 0; i < KS; ++i) {
@@ -461,66 +690,39 @@ __global__ void __launch_bounds__(kThreads)
                     o[i][3] *= al1;
                 }
             }
-            // P^T as the B operand: transpose the two 8x8 halves of P
-            const uint32_t pb0 = ptx::movmatrix_t(pack_half2(p0 * sv, p1 * sv));
-            const uint32_t pb1 = ptx::movmatrix_t(pack_half2(p2 * sv, p3 * sv));
-
-            // ---- O^T += V_page^T . P^T
-            if constexpr (!kInt8) {
-                const int lt = (lane & 7) + 8 * (lane >> 4);
-                const int lch = (lane >> 3) & 1;
-                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                if (ntok < kPage) {  // NaN-safe: zero V rows of tokens past the end
-                    mlo = (2 * c < ntok ? 0x0000ffffu : 0u) | (2 * c + 1 < ntok ? 0xffff0000u : 0u);
-                    mhi = (2 * c + 8 < ntok ? 0x0000ffffu : 0u) |
-                          (2 * c + 9 < ntok ? 0xffff0000u : 0u);
-                }
+            // ---- O^T += V^T . P^T per page (P^T: transposed 8x8 halves of P)
 #pragma unroll
-                for (int i = 0; i < KS; ++i) {
-                    uint32_t a0, a1, a2, a3;
-                    ptx::ldsm_x4_t(vt + swz<C::kRowBytes>(lt, 2 * i + lch), a0, a1, a2, a3);
-                    ptx::mma_16816(o[i], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
-                }
-            } else {
-                // lane (g, c): tokens 2c, 2c+1, 2c+8, 2c+9; bytes [DG*g, DG*g + DG), DG = kD/8
-                constexpr int NW = kD / 32;  // words per token per lane
-                uint32_t vw[4][NW];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int t = 2 * c + (r & 1) + 8 * (r >> 1);
-                    if constexpr (kD == 128) {
-                        const uint4 v = ptx::lds128(vt + swz<C::kRowBytes>(t, g));
-                        vw[r][0] = v.x ^ 0x80808080u;
-                        vw[r][1] = v.y ^ 0x80808080u;
-                        vw[r][2] = v.z ^ 0x80808080u;
-                        vw[r][3] = v.w ^ 0x80808080u;
-                    } else {
-                        const uint2 v = ptx::lds64(vt + swz<C::kRowBytes>(t, g >> 1) + (g & 1) * 8);
-                        vw[r][0] = v.x ^ 0x80808080u;
-                        vw[r][1] = v.y ^ 0x80808080u;
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < KS; ++i) {
-                    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-                    const uint32_t il01 = ptx::prmt(vw[0][i >> 1], vw[1][i >> 1], sel);
-                    const uint32_t il23 = ptx::prmt(vw[2][i >> 1], vw[3][i >> 1], sel);
-                    ptx::mma_16816(o[i], i8pair_to_h2(il01, 0x4140u), i8pair_to_h2(il01, 0x4342u),
-                                   i8pair_to_h2(il23, 0x4140u), i8pair_to_h2(il23, 0x4342u), pb0,
-                                   pb1);
+            for (int u = 0; u < PPS; ++u) {
+                if (good[u]) {
+                    float sv = 1.f;
+                    if constexpr (kInt8) sv = hf[4 + u];
+                    const uint32_t pb0 =
+                        ptx::movmatrix_t(pack_half2(pr[u][0] * sv, pr[u][1] * sv));
+                    const uint32_t pb1 =
+                        ptx::movmatrix_t(pack_half2(pr[u][2] * sv, pr[u][3] * sv));
+                    const int ntok = min(kPage, ctx - (cc.page + u) * kPage);
+                    page_pv<kInt8, kD>(st + u * C::kPageBytes + C::kTileBytes, pb0, pb1, ntok,
+                                       lane, o);
                 }
             }
         }
         __syncwarp();
 
-        // ---- refill this stage with the page S ahead
-        if (k + S < n) {
+        // ---- refill this stage with the next pages
+        if (ipos < n) {
+            const int icnt = ci.unit(PPS, n - ipos);
+            int32_t blk[PPS];
+#pragma unroll
+            for (int u = 0; u < PPS; ++u) blk[u] = __shfl_sync(0xffffffffu, nblk, u);
             if (lane == 0) {
                 ptx::fence_proxy_async_smem();
-                issue(slot, nblk, ci.item / p.qgroups);
+                issue(slot, icnt, blk, ci.item / p.qgroups);
             }
-            ci.next(p, prefix);
-            if (lane == 0 && k + S + 1 < n) nblk = __ldg(p.block_tables + ci.seq * mb + ci.page);
+            ci.advance(p, prefix, icnt);
+            ipos += icnt;
+            ++issued;
+            if (ipos < n && lane < ci.unit(PPS, n - ipos))
+                nblk = __ldg(p.block_tables + ci.seq * mb + ci.page + lane);
         }
 
         // ---- piece finished: final output, or a partial for the reduce
@@ -530,7 +732,7 @@ __global__ void __launch_bounds__(kThreads)
                 l0 += __shfl_xor_sync(0xffffffffu, l0, off);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, off);
             }
-            const bool whole = piece_first_page == 0 && cc.page == cc.npages - 1;
+            const bool whole = piece_first_page == 0 && cc.page + cnt == cc.npages;
             const int hA = 2 * c, hB = 2 * c + 1;
             float *dstA, *dstB;
             float fA, fB;
@@ -562,6 +764,14 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             }
+            if (!whole && piece_first_page == 0 && lane == 0) {
+                // this piece starts an item that later workers continue
+                const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[cc.seq] +
+                                   static_cast<int64_t>(cc.item) * cc.npages;
+                write_split(p, w, true, piece_has_a ? 0 : 1,
+                            worker_of(s0 + cc.npages - 1, total, p.num_workers), cc.seq, cc.item,
+                            total);
+            }
             if constexpr (!kInt8) {
 #pragma unroll
                 for (int i = 0; i < KS; ++i) {
@@ -589,67 +799,119 @@ __global__ void __launch_bounds__(kThreads)
                 }
             }
         }
-        cc.next(p, prefix);
+        cc.advance(p, prefix, cnt);
+        pos += cnt;
     }
 }
 
-// Split-context reduce: one warp per item that more than one worker touched.
-// out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w with M = max_w m_w;
-// a piece flagged bad (l < 0) zeroes the item.
+// Split-context reduce: one warp per (worker, query head).  A worker whose
+// range holds the first piece of a split item merges that item:
+//   out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w,  M = max_w m_w
+// over the pieces of workers first .. last.  A piece flagged bad (l < 0)
+// zeroes the item.  The lanes read the (m, l) of up to 32 pieces at once,
+// then the accumulators of four pieces per batch, lanes across head_dim,
+// pieces in a fixed order.
 template <int kD>
 __global__ void __launch_bounds__(kThreads) reduce_kernel(const DecodeArgs p)
 {
-    extern __shared__ int32_t tabs[];
-    int32_t *prefix = tabs;
-    int32_t *ctxs = prefix + p.num_seqs + 1;
-    build_page_tables(p, prefix, ctxs);
-    const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t it = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-    if (total == 0 || it >= static_cast<int64_t>(p.num_seqs) * p.items_per_seq) return;
-    const int seq = static_cast<int>(it / p.items_per_seq);
-    const int item = static_cast<int>(it % p.items_per_seq);
-    const int np = prefix[seq + 1] - prefix[seq];
-    if (np == 0) return;
-    const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[seq] +
-                       static_cast<int64_t>(item) * np;
-    const int64_t e0 = s0 + np;
-    const int W = p.num_workers;
-    const int64_t wf = worker_of(s0, total, W), wl = worker_of(e0 - 1, total, W);
-    if (wf == wl) return;  // finished in place by one worker
+    ptx::griddep_wait();  // the decode grid's records are complete and visible
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const int wf = static_cast<int>(gw / p.rec_heads);
+    const int h = static_cast<int>(gw - static_cast<int64_t>(wf) * p.rec_heads);
+    if (wf >= p.num_workers) return;
+    const int4 d0 = __ldcg(p.splits + 2 * wf);
+    if (!(d0.x & 1)) return;
+    const int seq = d0.z, item = d0.w;
     const int kvh = item / p.qgroups, qg = item - kvh * p.qgroups;
     const int h0 = kvh * p.group + qg * kItemHeads;
     const int gh = min(kItemHeads, p.group - qg * kItemHeads);
-    for (int h = 0; h < gh; ++h) {
-        float M = -INFINITY;
-        bool bad = false;
-        for (int64_t w = wf; w <= wl; ++w) {
-            const int64_t aw = w * total / W;
-            if (aw == (w + 1) * total / W) continue;  // worker with no pages
-            const int slot = s0 <= aw ? 0 : 1;
-            const float *rec = p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
-            M = fmaxf(M, rec[0]);
-            bad |= rec[1] < 0.f;
+    if (h >= gh) return;
+    const int nw = d0.y - wf + 1;
+    const int slot0 = (d0.x >> 1) & 1;
+    const bool dense = (d0.x & 4) != 0;
+    const int64_t total = dense ? 0 : __ldcg(p.splits + 2 * wf + 1).x;
+    const int W = p.num_workers;
+
+    // the record of piece j of this item (null: a worker with no pages)
+    auto rec_of = [&](int j) -> const float * {
+        const int64_t w = wf + j;
+        if (!dense && j > 0 && w * total / W == (w + 1) * total / W) return nullptr;
+        const int slot = j == 0 ? slot0 : 0;
+        return p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
+    };
+
+    float M = -INFINITY;
+    bool bad = false;
+    for (int base = 0; base < nw; base += 32) {
+        const float *r = base + lane < nw ? rec_of(base + lane) : nullptr;
+        if (r) {
+            M = fmaxf(M, __ldcg(r));
+            bad |= __ldcg(r + 1) < 0.f;
         }
-        float acc[kD / 32];
-#pragma unroll
-        for (int j = 0; j < kD / 32; ++j) acc[j] = 0.f;
-        float L = 0.f;
-        for (int64_t w = wf; w <= wl; ++w) {
-            const int64_t aw = w * total / W;
-            if (aw == (w + 1) * total / W) continue;
-            const int slot = s0 <= aw ? 0 : 1;
-            const float *rec = p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
-            const float f = ptx::ex2(rec[0] - M);
-            L += f * rec[1];
-#pragma unroll
-            for (int j = 0; j < kD / 32; ++j) acc[j] += f * rec[4 + lane + 32 * j];
-        }
-        float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
-        const float inv = bad ? 0.f : 1.f / L;
-#pragma unroll
-        for (int j = 0; j < kD / 32; ++j) dst[lane + 32 * j] = bad ? 0.f : acc[j] * inv;
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    bad = __any_sync(0xffffffffu, bad);
+
+    float acc[kD / 32];
+#pragma unroll
+    for (int i = 0; i < kD / 32; ++i) acc[i] = 0.f;
+    float L = 0.f;
+    for (int base = 0; base < nw; base += 32) {
+        const float *mine = base + lane < nw ? rec_of(base + lane) : nullptr;
+        const float f_lane = mine ? ptx::ex2(__ldcg(mine) - M) : 0.f;
+        if (mine) L += f_lane * __ldcg(mine + 1);
+        const uint64_t mbits = reinterpret_cast<uint64_t>(mine);
+        const uint32_t mlo = static_cast<uint32_t>(mbits), mhi = static_cast<uint32_t>(mbits >> 32);
+        const int cnt = min(32, nw - base);
+        for (int j0 = 0; j0 < cnt; j0 += 4) {
+            float v[4][kD / 32], f[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int src = min(j0 + u, 31);
+                const uint64_t bits =
+                    (static_cast<uint64_t>(__shfl_sync(0xffffffffu, mhi, src)) << 32) |
+                    __shfl_sync(0xffffffffu, mlo, src);
+                f[u] = __shfl_sync(0xffffffffu, f_lane, src);
+                const float *r = reinterpret_cast<const float *>(bits);
+                const bool use = j0 + u < cnt && r != nullptr;
+                if (!use) f[u] = 0.f;
+#pragma unroll
+                for (int i = 0; i < kD / 32; ++i) v[u][i] = use ? __ldcg(r + 4 + lane + 32 * i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int i = 0; i < kD / 32; ++i) acc[i] += f[u] * v[u][i];
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
+    const float inv = bad ? 0.f : 1.f / L;
+#pragma unroll
+    for (int i = 0; i < kD / 32; ++i) dst[lane + 32 * i] = bad ? 0.f : acc[i] * inv;
+}
+
+// Launch with programmatic stream serialisation: the kernel may begin while
+// the previous kernel on the stream drains; it calls griddepcontrol.wait
+// before touching that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t st, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ------------------------------------------------------------------- host
@@ -700,10 +962,18 @@ pkv_status check_shape(int num_seqs, int num_heads, int num_kv_heads, int head_d
     return PKV_OK;
 }
 
-size_t workspace_bytes_for(const Shape &sh, int head_dim)
+// workspace: the partial records of up to min(4096, pages) workers, then
+// two int4 split descriptors per worker
+size_t partial_bytes_for(const Shape &sh, int head_dim)
 {
     const int64_t workers = sh.max_pages < kMaxWorkers ? sh.max_pages : kMaxWorkers;
     return static_cast<size_t>(workers) * 2 * sh.rec_heads * (head_dim + 4) * sizeof(float);
+}
+
+size_t workspace_bytes_for(const Shape &sh, int head_dim)
+{
+    const int64_t workers = sh.max_pages < kMaxWorkers ? sh.max_pages : kMaxWorkers;
+    return partial_bytes_for(sh, head_dim) + static_cast<size_t>(workers) * 2 * sizeof(int4);
 }
 
 struct OccCache {
@@ -723,6 +993,7 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     auto kern = decode_kernel<kInt8, kD>;
     static OccCache occ[64];
     int per_sm = 0;
+    int cap = 0;
     {
         std::lock_guard<std::mutex> lock(g_cfg_mu);
         OccCache &oc = occ[di.device & 63];
@@ -739,11 +1010,12 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
             oc.per_sm = v;
         }
         per_sm = oc.per_sm;
+        cap = g_worker_cap;
     }
     if (per_sm <= 0) return PKV_ERR_UNSUPPORTED;
     int64_t workers = static_cast<int64_t>(per_sm) * di.num_sms * kWarps;
     if (workers > kMaxWorkers) workers = kMaxWorkers;
-    if (g_worker_cap > 0 && workers > g_worker_cap) workers = g_worker_cap;
+    if (cap > 0 && workers > cap) workers = cap;
     if (workers > sh.max_pages) workers = sh.max_pages;
     if (workers < 1) workers = 1;
 
@@ -761,6 +1033,8 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     args.k_scales = call.k_scales;
     args.v_scales = call.v_scales;
     args.partials = static_cast<float *>(call.workspace);
+    args.splits = reinterpret_cast<int4 *>(static_cast<uint8_t *>(call.workspace) +
+                                           partial_bytes_for(sh, call.head_dim));
     args.dev_status = call.dev_status;
     args.num_seqs = call.num_seqs;
     args.num_heads = call.num_heads;
@@ -776,21 +1050,19 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     args.scale_log2 = call.softmax_scale * 1.4426950408889634f;
 
     cudaStream_t st = static_cast<cudaStream_t>(call.stream);
-    const int grid = static_cast<int>((workers + kWarps - 1) / kWarps);
-    kern<<<grid, kThreads, smem, st>>>(args, tmk, tmv);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    const unsigned grid = static_cast<unsigned>((workers + kWarps - 1) / kWarps);
+    if (launch_pdl(kern, grid, kThreads, smem, st, args, tmk, tmv) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
     if (workers > 1) {
-        const size_t rsmem = static_cast<size_t>(2 * call.num_seqs + 1) * sizeof(int32_t);
-        const int64_t items = static_cast<int64_t>(call.num_seqs) * sh.items_per_seq;
-        const int64_t rgrid = (items + kWarps - 1) / kWarps;
-        if (rgrid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+        const int64_t warps = workers * sh.rec_heads;
+        const int64_t rgrid = (warps + kWarps - 1) / kWarps;
         auto rk = reduce_kernel<kD>;
-        if (rsmem > 48 * 1024 &&
-            cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(rsmem)) != cudaSuccess)
+        if (launch_pdl(rk, static_cast<unsigned>(rgrid), kThreads, 0, st, args) != cudaSuccess) {
+            cudaGetLastError();
             return PKV_ERR_CUDA;
-        rk<<<static_cast<unsigned>(rgrid), kThreads, rsmem, st>>>(args);
-        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        }
     }
     return PKV_OK;
 }

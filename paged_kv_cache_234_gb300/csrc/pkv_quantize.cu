@@ -12,16 +12,30 @@
 #include <stdint.h>
 
 #include "pkv_host.cuh"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kQuantWarps = 8;
+constexpr int kQuantWarps = 4;
 
-__device__ __forceinline__ int quant_code(float x, float scale)
+// code = round-half-even(fl32(x / scale)), clamped to [-127, 127]; a NaN
+// quotient gives 0.  y' = x * fl32(1/scale) is within 2 ulp of fl32(x/scale);
+// ulp <= 2^-17 for |x/scale| <= 127, so when y' is more than 2^-14 away from
+// every half-integer both round to the same integer.  Only quotients that
+// close to a tie (and NaN/inf cases) take the IEEE division.
+__device__ __forceinline__ int quant_code(float x, float scale, float rcp)
 {
-    const float y = __fdiv_rn(x, scale);
-    if (isnan(y)) return 0;  // 0/0, inf/inf or a NaN input
+    const float yf = x * rcp;
+    const float r = rintf(yf);
+    float y;
+    if (fabsf(yf - r) < 0.5f - 0.00006103515625f) {  // 0.5 - 2^-14; false for NaN
+        y = r;
+    } else {
+        y = __fdiv_rn(x, scale);
+        if (isnan(y)) return 0;  // 0/0, inf/inf or a NaN input
+        y = rintf(y);
+    }
     int c = __float2int_rn(y);
     c = c > 127 ? 127 : c;
     c = c < -127 ? -127 : c;
@@ -39,6 +53,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 {
     constexpr int kTileElems = 16 * kHeadDim;
     constexpr int kChunks = kTileElems / 8 / 32;  // 16-byte chunks per lane
+    // programmatic dependent launch: the previous kernel's writes (and its
+    // reads of the pools this kernel overwrites) are complete past this point
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
     if (gwarp >= 2 * tiles_per_pool) return;
@@ -73,6 +91,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float scale = __fdiv_rn(amax, 127.0f);
+    const float rcp = __frcp_rn(scale);
 
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
@@ -82,10 +101,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         for (int w = 0; w < 2; ++w) {
             const float2 f0 = __half22float2(p[2 * w]);
             const float2 f1 = __half22float2(p[2 * w + 1]);
-            const uint32_t b0 = static_cast<uint32_t>(quant_code(f0.x, scale)) & 0xffu;
-            const uint32_t b1 = static_cast<uint32_t>(quant_code(f0.y, scale)) & 0xffu;
-            const uint32_t b2 = static_cast<uint32_t>(quant_code(f1.x, scale)) & 0xffu;
-            const uint32_t b3 = static_cast<uint32_t>(quant_code(f1.y, scale)) & 0xffu;
+            const uint32_t b0 = static_cast<uint32_t>(quant_code(f0.x, scale, rcp)) & 0xffu;
+            const uint32_t b1 = static_cast<uint32_t>(quant_code(f0.y, scale, rcp)) & 0xffu;
+            const uint32_t b2 = static_cast<uint32_t>(quant_code(f1.x, scale, rcp)) & 0xffu;
+            const uint32_t b3 = static_cast<uint32_t>(quant_code(f1.y, scale, rcp)) & 0xffu;
             packed[w] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
         }
         __stcs(dst + c * 32 + lane, make_uint2(packed[0], packed[1]));
@@ -120,14 +139,26 @@ extern "C" pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16
     if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 g(static_cast<unsigned>(grid)), b(kQuantWarps * 32);
-    if (head_dim == 128) {
-        quantize_kernel<128><<<g, b, 0, s>>>(
-            static_cast<const __half *>(k_fp16), static_cast<const __half *>(v_fp16), k_codes,
-            v_codes, k_scales, v_scales, block_ids, tiles, num_kv_heads, num_blocks, dev_status);
-    } else {
-        quantize_kernel<64><<<g, b, 0, s>>>(
-            static_cast<const __half *>(k_fp16), static_cast<const __half *>(v_fp16), k_codes,
-            v_codes, k_scales, v_scales, block_ids, tiles, num_kv_heads, num_blocks, dev_status);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = g;
+    cfg.blockDim = b;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const __half *kin = static_cast<const __half *>(k_fp16);
+    const __half *vin = static_cast<const __half *>(v_fp16);
+    const cudaError_t e =
+        head_dim == 128
+            ? cudaLaunchKernelEx(&cfg, quantize_kernel<128>, kin, vin, k_codes, v_codes, k_scales,
+                                 v_scales, block_ids, tiles, num_kv_heads, num_blocks, dev_status)
+            : cudaLaunchKernelEx(&cfg, quantize_kernel<64>, kin, vin, k_codes, v_codes, k_scales,
+                                 v_scales, block_ids, tiles, num_kv_heads, num_blocks, dev_status);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
     }
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return PKV_OK;
 }

@@ -48,12 +48,15 @@ def test_status_strings(L):
 
 
 def test_workspace_size_arithmetic(L):
-    # two partial records per worker, min(8, group) heads each, (d + 4) floats
-    # per record; at most 4096 workers and never more than the pages.
-    assert pkv.pkv_decode_workspace_size(64, 32, 8, 128, 2048) == 4096 * 2 * 4 * 132 * 4
-    assert pkv.pkv_decode_workspace_size(2, 8, 2, 64, 37) == (2 * 2 * 3) * 2 * 4 * 68 * 4
-    assert pkv.pkv_decode_workspace_size(8, 8, 8, 128, 512) == 2048 * 2 * 1 * 132 * 4
-    assert pkv.pkv_decode_workspace_size(1, 32, 1, 128, 16) == 4 * 2 * 8 * 132 * 4
+    # per worker: two partial records of min(8, group) heads x (d + 4) floats
+    # and two 16-byte split descriptors; at most 4096 workers and never more
+    # than the pages.
+    def expect(workers, heads, d):
+        return workers * (2 * heads * (d + 4) * 4 + 32)
+    assert pkv.pkv_decode_workspace_size(64, 32, 8, 128, 2048) == expect(4096, 4, 128)
+    assert pkv.pkv_decode_workspace_size(2, 8, 2, 64, 37) == expect(2 * 2 * 3, 4, 64)
+    assert pkv.pkv_decode_workspace_size(8, 8, 8, 128, 512) == expect(2048, 1, 128)
+    assert pkv.pkv_decode_workspace_size(1, 32, 1, 128, 16) == expect(4, 8, 128)
     assert pkv.pkv_decode_workspace_size(4, 8, 3, 128, 16) == 0      # heads not divisible
     assert pkv.pkv_decode_workspace_size(4, 8, 2, 96, 16) == 0       # unsupported head_dim
     assert pkv.pkv_decode_workspace_size(0, 8, 2, 64, 0) == 0
