@@ -160,6 +160,42 @@ PKV_API pkv_status pkv_paged_decode_int8(float *out, const void *query,
                                  int32_t *dev_status, void *stream);
 
 /*
+ * pkv_paged_decode_int8_static_workspace -- pkv_paged_decode_int8 for
+ * callers that cannot allocate device memory.  This call has no counterpart
+ * in the source pages: it serves code whose device memory is owned by some
+ * other allocator (a framework pool that must see every allocation), and
+ * code that cannot afford the implicit device synchronisation that
+ * cudaMalloc / cudaFree may perform.  Such callers cannot provide the
+ * workspace argument, so this variant uses a fixed scratch array of
+ * PKV_STATIC_WORKSPACE_BYTES compiled into the library instead.
+ *
+ * Everything else -- arguments, layouts, results, error codes -- is as for
+ * pkv_paged_decode_int8, without workspace / workspace_bytes.  The library
+ * allocates nothing here (no cudaMalloc, no cudaFree, no allocating
+ * library routine):
+ *  - the scratch array is part of the library's device image, so every GPU
+ *    that loads the library holds PKV_STATIC_WORKSPACE_BYTES until exit;
+ *  - the first call on each device looks up the array's device address
+ *    (with that device current); make that first call before any stream
+ *    capture begins;
+ *  - a call whose workspace requirement (pkv_decode_workspace_size) exceeds
+ *    PKV_STATIC_WORKSPACE_BYTES returns PKV_ERR_WORKSPACE without launching;
+ *  - all calls on a device share the one array: calls that can overlap on
+ *    the GPU (different streams, no ordering between them) race and give
+ *    wrong results.  The array needs no clearing: each call rewrites what it
+ *    reads.
+ */
+#define PKV_STATIC_WORKSPACE_BYTES (32u << 20)
+
+PKV_API pkv_status pkv_paged_decode_int8_static_workspace(
+    float *out, const void *query, const int8_t *k_codes, const int8_t *v_codes,
+    const float *k_scales, const float *v_scales, int num_blocks,
+    const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size,
+    float softmax_scale, int32_t *dev_status, void *stream);
+
+/*
  * Bytes of workspace a decode call with these sizes needs (either variant).
  * Pure host arithmetic: no CUDA call.  Returns 0 for invalid sizes.
  */

@@ -36,7 +36,11 @@ PKV_DEV_BAD_CTX = 2
 PKV_DEV_TIMEOUT = 4
 
 EXPORTED = ("pkv_quantize_blocks", "pkv_paged_decode_fp16", "pkv_paged_decode_int8",
-            "pkv_decode_workspace_size", "pkv_set_decode_workers", "pkv_status_string")
+            "pkv_paged_decode_int8_static_workspace", "pkv_decode_workspace_size",
+            "pkv_set_decode_workers", "pkv_status_string")
+
+# size of the scratch array behind pkv_paged_decode_int8_static_workspace
+PKV_STATIC_WORKSPACE_BYTES = 32 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_paged_decode_fp16.argtypes = dec
         L.pkv_paged_decode_int8.restype = I
         L.pkv_paged_decode_int8.argtypes = dec[:4] + [P, P] + dec[4:]
+        L.pkv_paged_decode_int8_static_workspace.restype = I
+        L.pkv_paged_decode_int8_static_workspace.argtypes = dec[:4] + [P, P] + dec[4:15] + dec[17:]
         L.pkv_decode_workspace_size.restype = Z
         L.pkv_decode_workspace_size.argtypes = [I, I, I, I, I]
         L.pkv_set_decode_workers.restype = I
@@ -191,3 +197,30 @@ def decode_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_context_le
     nbytes = pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
                                        max_context_len)
     return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def pkv_paged_decode_int8_static_workspace(out, query, k_codes, v_codes, k_scales, v_scales,
+                                           block_tables, context_lens, max_context_len,
+                                           softmax_scale, dev_status=None, stream=None) -> None:
+    """INT8 decode for callers that cannot allocate: the scratch is a fixed
+    array inside the library (PKV_STATIC_WORKSPACE_BYTES per device).  Calls
+    that may overlap on the GPU must not use it concurrently."""
+    import torch
+    _check(out, "out", torch.float32)
+    _check(query, "query", torch.float16)
+    _check(k_codes, "k_codes", torch.int8)
+    _check(v_codes, "v_codes", torch.int8)
+    _check(k_scales, "k_scales", torch.float32)
+    _check(v_scales, "v_scales", torch.float32)
+    _check(block_tables, "block_tables", torch.int32)
+    _check(context_lens, "context_lens", torch.int32)
+    _check(dev_status, "dev_status", torch.int32)
+    n, hq, d = query.shape
+    nb, hkv, bs, _ = k_codes.shape
+    mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    st = lib().pkv_paged_decode_int8_static_workspace(
+        _ptr(out), _ptr(query), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales),
+        nb, _ptr(block_tables), mb, _ptr(context_lens), int(max_context_len), n, hq, hkv, d, bs,
+        float(softmax_scale), _ptr(dev_status), _stream(stream))
+    if st != PKV_OK:
+        raise PkvError(st, "pkv_paged_decode_int8_static_workspace")

@@ -1156,3 +1156,51 @@ extern "C" pkv_status pkv_set_decode_workers(int max_workers)
     pkv::g_worker_cap = max_workers;
     return PKV_OK;
 }
+
+// ------------------------------------------------- decode without allocation
+// Scratch for pkv_paged_decode_int8_static_workspace: a fixed device array
+// that every GPU loading this library holds until the process exits.  Only
+// the partial records and split descriptors of the decode live here; they are
+// fully rewritten by every call before they are read, so nothing needs to
+// start at zero.  Host code must not pass `g_static_ws` itself to a kernel:
+// on the host that name is a stand-in, not a device address.
+static __device__ __align__(256) unsigned char g_static_ws[PKV_STATIC_WORKSPACE_BYTES];
+
+namespace pkv {
+namespace {
+std::mutex g_static_mu;
+void *g_static_ptr[64] = {};  // device address of g_static_ws, per device
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_decode_int8_static_workspace(
+    float *out, const void *query, const int8_t *k_codes, const int8_t *v_codes,
+    const float *k_scales, const float *v_scales, int num_blocks, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, float softmax_scale,
+    int32_t *dev_status, void *stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+    void *ws = nullptr;
+    {
+        // set-up, once per device, with that device current
+        std::lock_guard<std::mutex> lock(pkv::g_static_mu);
+        if (!pkv::g_static_ptr[dev]) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) {
+                cudaGetLastError();
+                return PKV_ERR_CUDA;
+            }
+            pkv::g_static_ptr[dev] = ptr;
+        }
+        ws = pkv::g_static_ptr[dev];
+    }
+    const pkv::DecodeCall call{out, query, k_codes, v_codes, k_scales, v_scales, num_blocks,
+                               block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                               num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                               softmax_scale, ws, PKV_STATIC_WORKSPACE_BYTES, dev_status, stream};
+    // a call needing more than PKV_STATIC_WORKSPACE_BYTES of scratch is
+    // rejected with PKV_ERR_WORKSPACE before anything is launched
+    return pkv::decode_entry(call, true);
+}
