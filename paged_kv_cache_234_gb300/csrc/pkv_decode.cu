@@ -207,6 +207,8 @@ __device__ void build_page_tables(const DecodeArgs &p, int32_t *prefix, int32_t 
 struct PageCursor {
     int seq;     // sequence
     int item;    // kv head * qgroups + query-head group
+    int kvh;     // kv head of the item
+    int qg;      // query-head group of the item (8 heads each)
     int page;    // page (16-token block) within the sequence
     int npages;  // pages of the sequence
 
@@ -225,9 +227,11 @@ struct PageCursor {
         const int64_t r = x - static_cast<int64_t>(p.items_per_seq) * prefix[lo];
         item = static_cast<int>(r / npages);
         page = static_cast<int>(r % npages);
+        kvh = item / p.qgroups;
+        qg = item - kvh * p.qgroups;
     }
 
-    // pages of the next stage: up to kPPS, never past the item's end or `left`
+    // pages of the next stage: up to pps, never past the item's end or `left`
     __device__ __forceinline__ int unit(int pps, int left) const
     {
         int u = npages - page;
@@ -240,8 +244,12 @@ struct PageCursor {
         page += k;
         if (page < npages) return;
         page = 0;
+        if (++qg == p.qgroups) {
+            qg = 0;
+            ++kvh;
+        }
         if (++item < p.items_per_seq) return;
-        item = 0;
+        item = kvh = qg = 0;
         do {
             ++seq;
         } while (seq < p.num_seqs && prefix[seq + 1] == prefix[seq]);
@@ -505,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
             const int cnt = cj.unit(PPS, n - pos);
             if (j == my_stage) {
                 mycnt = cnt;
-                mykvh = cj.item / p.qgroups;
+                mykvh = cj.kvh;
                 if (my_u < cnt) myblk = __ldg(p.block_tables + cj.seq * mb + cj.page + my_u);
             }
             cj.advance(p, prefix, cnt);
@@ -546,10 +554,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
         const int cnt = cc.unit(PPS, n - pos);
         const bool first = pos == 0 || cc.page == 0;
         const bool last = pos + cnt == n || cc.page + cnt == cc.npages;
-        const int kvh = cc.item / p.qgroups;
-        const int qg = cc.item - kvh * p.qgroups;
-        const int h0 = kvh * p.group + qg * kItemHeads;
-        const int gh = min(kItemHeads, p.group - qg * kItemHeads);
+        const int h0 = cc.kvh * p.group + cc.qg * kItemHeads;
+        const int gh = min(kItemHeads, p.group - cc.qg * kItemHeads);
 
         if (first) {
             // query fragments of the item's heads; heads past gh are zero
@@ -716,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
             for (int u = 0; u < PPS; ++u) blk[u] = __shfl_sync(0xffffffffu, nblk, u);
             if (lane == 0) {
                 ptx::fence_proxy_async_smem();
-                issue(slot, icnt, blk, ci.item / p.qgroups);
+                issue(slot, icnt, blk, ci.kvh);
             }
             ci.advance(p, prefix, icnt);
             ipos += icnt;
