@@ -814,9 +814,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
 // range holds the first piece of a split item merges that item:
 //   out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w,  M = max_w m_w
 // over the pieces of workers first .. last.  A piece flagged bad (l < 0)
-// zeroes the item.  The lanes read the (m, l) of up to 32 pieces at once,
-// then the accumulators of four pieces per batch, lanes across head_dim,
-// pieces in a fixed order.
+// zeroes the item.  With up to four pieces (the usual case) every load of
+// every piece is issued at once; otherwise lanes read the (m, l) of up to 32
+// pieces at a time, then the accumulators four pieces per batch.  Lanes run
+// across head_dim; pieces are combined in a fixed order.
 template <int kD>
 __global__ void __launch_bounds__(kThreads) reduce_kernel(const DecodeArgs p)
 {
@@ -847,53 +848,77 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const DecodeArgs p)
         return p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
     };
 
-    float M = -INFINITY;
-    bool bad = false;
-    for (int base = 0; base < nw; base += 32) {
-        const float *r = base + lane < nw ? rec_of(base + lane) : nullptr;
-        if (r) {
-            M = fmaxf(M, __ldcg(r));
-            bad |= __ldcg(r + 1) < 0.f;
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    bad = __any_sync(0xffffffffu, bad);
-
     float acc[kD / 32];
 #pragma unroll
     for (int i = 0; i < kD / 32; ++i) acc[i] = 0.f;
     float L = 0.f;
-    for (int base = 0; base < nw; base += 32) {
-        const float *mine = base + lane < nw ? rec_of(base + lane) : nullptr;
-        const float f_lane = mine ? ptx::ex2(__ldcg(mine) - M) : 0.f;
-        if (mine) L += f_lane * __ldcg(mine + 1);
-        const uint64_t mbits = reinterpret_cast<uint64_t>(mine);
-        const uint32_t mlo = static_cast<uint32_t>(mbits), mhi = static_cast<uint32_t>(mbits >> 32);
-        const int cnt = min(32, nw - base);
-        for (int j0 = 0; j0 < cnt; j0 += 4) {
-            float v[4][kD / 32], f[4];
+    bool bad = false;
+    if (nw <= 4) {
+        // common case: every load of every piece issued at once
+        float m[4], l[4], v[4][kD / 32];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int src = min(j0 + u, 31);
-                const uint64_t bits =
-                    (static_cast<uint64_t>(__shfl_sync(0xffffffffu, mhi, src)) << 32) |
-                    __shfl_sync(0xffffffffu, mlo, src);
-                f[u] = __shfl_sync(0xffffffffu, f_lane, src);
-                const float *r = reinterpret_cast<const float *>(bits);
-                const bool use = j0 + u < cnt && r != nullptr;
-                if (!use) f[u] = 0.f;
+        for (int j = 0; j < 4; ++j) {
+            const float *r = j < nw ? rec_of(j) : nullptr;
+            m[j] = r ? __ldcg(r) : -INFINITY;
+            l[j] = r ? __ldcg(r + 1) : 0.f;
 #pragma unroll
-                for (int i = 0; i < kD / 32; ++i) v[u][i] = use ? __ldcg(r + 4 + lane + 32 * i) : 0.f;
+            for (int i = 0; i < kD / 32; ++i) v[j][i] = r ? __ldcg(r + 4 + lane + 32 * i) : 0.f;
+        }
+        const float M = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float f = m[j] == -INFINITY ? 0.f : ptx::ex2(m[j] - M);
+            bad |= l[j] < 0.f;
+            L += f * l[j];
+#pragma unroll
+            for (int i = 0; i < kD / 32; ++i) acc[i] += f * v[j][i];
+        }
+    } else {
+        float M = -INFINITY;
+        for (int base = 0; base < nw; base += 32) {
+            const float *r = base + lane < nw ? rec_of(base + lane) : nullptr;
+            if (r) {
+                M = fmaxf(M, __ldcg(r));
+                bad |= __ldcg(r + 1) < 0.f;
             }
+        }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        bad = __any_sync(0xffffffffu, bad);
+        for (int base = 0; base < nw; base += 32) {
+            const float *mine = base + lane < nw ? rec_of(base + lane) : nullptr;
+            const float f_lane = mine ? ptx::ex2(__ldcg(mine) - M) : 0.f;
+            float Lp = mine ? f_lane * __ldcg(mine + 1) : 0.f;
 #pragma unroll
-                for (int i = 0; i < kD / 32; ++i) acc[i] += f[u] * v[u][i];
+            for (int off = 16; off > 0; off >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, off);
+            L += Lp;
+            const uint64_t mbits = reinterpret_cast<uint64_t>(mine);
+            const uint32_t mlo = static_cast<uint32_t>(mbits);
+            const uint32_t mhi = static_cast<uint32_t>(mbits >> 32);
+            const int cnt = min(32, nw - base);
+            for (int j0 = 0; j0 < cnt; j0 += 4) {
+                float v[4][kD / 32], f[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int src = min(j0 + u, 31);
+                    const uint64_t bits =
+                        (static_cast<uint64_t>(__shfl_sync(0xffffffffu, mhi, src)) << 32) |
+                        __shfl_sync(0xffffffffu, mlo, src);
+                    f[u] = __shfl_sync(0xffffffffu, f_lane, src);
+                    const float *r = reinterpret_cast<const float *>(bits);
+                    const bool use = j0 + u < cnt && r != nullptr;
+                    if (!use) f[u] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < kD / 32; ++i)
+                        v[u][i] = use ? __ldcg(r + 4 + lane + 32 * i) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int i = 0; i < kD / 32; ++i) acc[i] += f[u] * v[u][i];
+            }
         }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
     const float inv = bad ? 0.f : 1.f / L;
 #pragma unroll

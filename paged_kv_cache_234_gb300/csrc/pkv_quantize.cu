@@ -2,12 +2,14 @@
 // K and V tiles (PagedKV-Fusion README, "Overview" component B and the
 // "Architecture" sequence diagram step "INT8 survivors + scales").
 //
-// One warp per (block, kv head, K|V) tile of 16 x head_dim fp16 values.  The
-// tile is read once with 16-byte loads (coalesced across the warp), max |x|
-// is reduced with warp shuffles, scale = max / 127 with an IEEE fp32
-// division, and every code is the half-even rounding of the IEEE fp32
-// quotient x / scale.  HBM-bound: 2 bytes read and 1 byte written per value,
-// plus 4 bytes of scale per tile.
+// One 128-thread CTA per (block, kv head, K|V) tile of 16 x head_dim fp16
+// values (grid-strided when there are many tiles).  The tile is read once with
+// 16-byte loads (coalesced), max |x| is reduced with warp shuffles and shared
+// memory, scale = max / 127 with an IEEE fp32 division, and every code is the
+// half-even rounding of the IEEE fp32 quotient x / scale.  HBM-bound for large
+// jobs: 2 bytes read and 1 byte written per value, plus 4 bytes of scale per
+// tile; for a decode step's few tail blocks it is latency-bound, hence the
+// many threads per tile.
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -17,7 +19,11 @@
 namespace pkv {
 namespace {
 
-constexpr int kQuantWarps = 4;
+constexpr int kQuantThreads = 128;  // one CTA per (block, kv head, K|V) tile
+
+// RNE(y) for |y| < 2^22 by the exact add of 1.5 * 2^23: the fp32 sum rounds
+// to nearest even at unit spacing; its low bits then hold the integer.
+constexpr float kRoundMagic = 12582912.0f;
 
 // code = round-half-even(fl32(x / scale)), clamped to [-127, 127]; a NaN
 // quotient gives 0.  y' = x * fl32(1/scale) is within 2 ulp of fl32(x/scale);
@@ -27,24 +33,21 @@ constexpr int kQuantWarps = 4;
 __device__ __forceinline__ int quant_code(float x, float scale, float rcp)
 {
     const float yf = x * rcp;
-    const float r = rintf(yf);
-    float y;
-    if (fabsf(yf - r) < 0.5f - 0.00006103515625f) {  // 0.5 - 2^-14; false for NaN
-        y = r;
-    } else {
-        y = __fdiv_rn(x, scale);
-        if (isnan(y)) return 0;  // 0/0, inf/inf or a NaN input
-        y = rintf(y);
+    const float t = yf + kRoundMagic;
+    const float r = t - kRoundMagic;
+    if (fabsf(yf - r) < 0.5f - 0.00006103515625f) {  // 0.5 - 2^-14; false for NaN/inf
+        return __float_as_int(t) - 0x4B400000;       // |r| <= 127: no clamp needed
     }
+    const float y = __fdiv_rn(x, scale);
+    if (isnan(y)) return 0;  // 0/0, inf/inf or a NaN input
     int c = __float2int_rn(y);
     c = c > 127 ? 127 : c;
     c = c < -127 ? -127 : c;
     return c;
 }
 
-// kChunks: 16-byte chunks of the tile handled by each lane.
 template <int kHeadDim>
-__global__ void __launch_bounds__(kQuantWarps * 32)
+__global__ void __launch_bounds__(kQuantThreads)
     quantize_kernel(const __half *__restrict__ k_in, const __half *__restrict__ v_in,
                     int8_t *__restrict__ k_out, int8_t *__restrict__ v_out,
                     float *__restrict__ k_scales, float *__restrict__ v_scales,
@@ -52,64 +55,73 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
                     int num_kv_heads, int num_blocks, int32_t *dev_status)
 {
     constexpr int kTileElems = 16 * kHeadDim;
-    constexpr int kChunks = kTileElems / 8 / 32;  // 16-byte chunks per lane
+    constexpr int kChunks = kTileElems / 8 / kQuantThreads;  // 16-byte chunks per thread
+    __shared__ float warp_max[kQuantThreads / 32];
     // programmatic dependent launch: the previous kernel's writes (and its
     // reads of the pools this kernel overwrites) are complete past this point
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
-    if (gwarp >= 2 * tiles_per_pool) return;
-    const bool is_v = gwarp >= tiles_per_pool;
-    const int64_t t = is_v ? gwarp - tiles_per_pool : gwarp;
-    const int64_t j = t / num_kv_heads;
-    const int h = static_cast<int>(t % num_kv_heads);
-    const int64_t blk = block_ids ? static_cast<int64_t>(block_ids[j]) : j;
-    if (blk < 0 || blk >= num_blocks) {
-        if (lane == 0 && h == 0 && !is_v && dev_status) atomicOr(dev_status, PKV_DEV_BAD_BLOCK);
-        return;
-    }
-    const int64_t tile = blk * num_kv_heads + h;
-    const uint4 *src = reinterpret_cast<const uint4 *>((is_v ? v_in : k_in) + tile * kTileElems);
-    uint2 *dst = reinterpret_cast<uint2 *>((is_v ? v_out : k_out) + tile * kTileElems);
-
-    uint4 raw[kChunks];
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) raw[c] = __ldcs(src + c * 32 + lane);
-
-    float amax = 0.0f;
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-        const __half2 *p = reinterpret_cast<const __half2 *>(&raw[c]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(p[e]);
-            amax = fmaxf(amax, fabsf(f.x));  // fmaxf drops a NaN operand
-            amax = fmaxf(amax, fabsf(f.y));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t task = blockIdx.x; task < 2 * tiles_per_pool; task += gridDim.x) {
+        const bool is_v = task >= tiles_per_pool;
+        const int64_t t = is_v ? task - tiles_per_pool : task;
+        const int64_t j = t / num_kv_heads;
+        const int h = static_cast<int>(t - j * num_kv_heads);
+        const int64_t blk = block_ids ? static_cast<int64_t>(__ldg(block_ids + j)) : j;
+        if (blk < 0 || blk >= num_blocks) {  // uniform across the CTA
+            if (threadIdx.x == 0 && h == 0 && !is_v && dev_status)
+                atomicOr(dev_status, PKV_DEV_BAD_BLOCK);
+            continue;
         }
-    }
+        const int64_t tile = blk * num_kv_heads + h;
+        const uint4 *src =
+            reinterpret_cast<const uint4 *>((is_v ? v_in : k_in) + tile * kTileElems);
+        uint2 *dst = reinterpret_cast<uint2 *>((is_v ? v_out : k_out) + tile * kTileElems);
+
+        uint4 raw[kChunks];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = __fdiv_rn(amax, 127.0f);
-    const float rcp = __frcp_rn(scale);
+        for (int c = 0; c < kChunks; ++c) raw[c] = __ldcs(src + c * kQuantThreads + threadIdx.x);
+
+        float amax = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+            const __half2 *hp = reinterpret_cast<const __half2 *>(&raw[c]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(hp[e]);
+                amax = fmaxf(amax, fabsf(f.x));  // fmaxf drops a NaN operand
+                amax = fmaxf(amax, fabsf(f.y));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) warp_max[warp] = amax;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+        __syncthreads();  // warp_max is reused by the next task
+        const float scale = __fdiv_rn(amax, 127.0f);
+        const float rcp = __frcp_rn(scale);
 
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-        const __half2 *p = reinterpret_cast<const __half2 *>(&raw[c]);
-        uint32_t packed[2];
+        for (int c = 0; c < kChunks; ++c) {
+            const __half2 *hp = reinterpret_cast<const __half2 *>(&raw[c]);
+            uint32_t packed[2];
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
-            const float2 f0 = __half22float2(p[2 * w]);
-            const float2 f1 = __half22float2(p[2 * w + 1]);
-            const uint32_t b0 = static_cast<uint32_t>(quant_code(f0.x, scale, rcp)) & 0xffu;
-            const uint32_t b1 = static_cast<uint32_t>(quant_code(f0.y, scale, rcp)) & 0xffu;
-            const uint32_t b2 = static_cast<uint32_t>(quant_code(f1.x, scale, rcp)) & 0xffu;
-            const uint32_t b3 = static_cast<uint32_t>(quant_code(f1.y, scale, rcp)) & 0xffu;
-            packed[w] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            for (int w = 0; w < 2; ++w) {
+                const float2 f0 = __half22float2(hp[2 * w]);
+                const float2 f1 = __half22float2(hp[2 * w + 1]);
+                const uint32_t b0 = static_cast<uint32_t>(quant_code(f0.x, scale, rcp)) & 0xffu;
+                const uint32_t b1 = static_cast<uint32_t>(quant_code(f0.y, scale, rcp)) & 0xffu;
+                const uint32_t b2 = static_cast<uint32_t>(quant_code(f1.x, scale, rcp)) & 0xffu;
+                const uint32_t b3 = static_cast<uint32_t>(quant_code(f1.y, scale, rcp)) & 0xffu;
+                packed[w] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            }
+            __stcs(dst + c * kQuantThreads + threadIdx.x, make_uint2(packed[0], packed[1]));
         }
-        __stcs(dst + c * 32 + lane, make_uint2(packed[0], packed[1]));
+        if (threadIdx.x == 0) (is_v ? v_scales : k_scales)[tile] = scale;
     }
-    if (lane == 0) (is_v ? v_scales : k_scales)[tile] = scale;
 }
 
 }  // namespace
@@ -134,11 +146,14 @@ extern "C" pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16
     const int64_t count = block_ids ? num_ids : num_blocks;
     const int64_t tiles = count * num_kv_heads;
     if (tiles == 0) return PKV_OK;
-    const int64_t warps = 2 * tiles;
-    const int64_t grid = (warps + kQuantWarps - 1) / kQuantWarps;
-    if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    // one CTA per tile, grid-strided beyond sixteen CTAs per SM
+    DeviceInfo di;
+    if (!current_device_info(&di)) return PKV_ERR_CUDA;
+    int64_t grid = 2 * tiles;
+    const int64_t cap = static_cast<int64_t>(di.num_sms) * 16;
+    if (grid > cap) grid = cap;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const dim3 g(static_cast<unsigned>(grid)), b(kQuantWarps * 32);
+    const dim3 g(static_cast<unsigned>(grid)), b(kQuantThreads);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = g;
     cfg.blockDim = b;
