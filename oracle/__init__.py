@@ -20,6 +20,16 @@ Every function cites the passage it follows:
   Overview component B; Architecture "per-block,head symmetric INT8"), with
   the absmax/127 scale and round-half-to-even reading.
 * ``kv_pool_mib`` -- the storage arithmetic of the Memory footprint table.
+* ``append_fp16`` / ``append_int8`` -- the write of one new token per
+  sequence at slot table[s][t / B] * B + t % B ("PagedAttention & KV-Cache
+  Memory Management", section 2.1 and the prefill step of its kernel
+  mechanics; section 3.3.2 "append the delta tokens"); the INT8 cache then
+  re-quantizes every tile it wrote with ``quantize``.
+* ``evict_scores`` / ``evict_select`` -- the least-reference-count + age
+  score of "PagedAttention & KV-Cache Memory Management", section 4.3.1
+  (alpha 0.7, beta 0.3), in fp32, and the choice of the k most evictable
+  blocks (PagedKV-Fusion README: score every physical block, return the
+  eviction ids).
 
 All functions here are pinned by tests in ``tests/test_oracle_pins.py``.
 """
@@ -77,6 +87,15 @@ def _load():
         lib.pkv_oracle_quantize.argtypes = [
             P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
             ctypes.c_int, ctypes.c_int]
+        lib.pkv_oracle_append.restype = ctypes.c_int64
+        lib.pkv_oracle_append.argtypes = [
+            P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int64, P, P]
+        lib.pkv_oracle_evict_scores.restype = ctypes.c_int64
+        lib.pkv_oracle_evict_scores.argtypes = [
+            P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_float]
+        lib.pkv_oracle_evict_select.restype = ctypes.c_int64
+        lib.pkv_oracle_evict_select.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int64]
         lib.pkv_oracle_max_threads.restype = ctypes.c_int
         lib.pkv_oracle_max_threads.argtypes = []
         _lib = lib
@@ -197,3 +216,93 @@ def kv_pool_mib(num_blocks, num_heads, head_dim, kind, block_size=16):
     else:
         raise ValueError(kind)
     return nbytes / float(1 << 20)
+
+
+def append_fp16(k_pool, v_pool, k_new, v_new, block_tables, positions, *, inplace=False):
+    """Write one new token per sequence into fp16 K/V pools.
+
+    pools [NB][Hkv][B][d] fp16; k_new, v_new [N][Hkv][d] fp16; block_tables
+    [N][MB] int32; positions [N] int32 (token index of the new token, < 0 =
+    no token).  Returns (k_pool, v_pool, flags [N] uint32, written [N] int32
+    = physical block written or -1).  With ``inplace`` the given contiguous
+    fp16 pools are written.
+    """
+    lib = _load()
+    if inplace:
+        kp, vp = k_pool, v_pool
+        for a in (kp, vp):
+            assert a.flags.c_contiguous and a.dtype == np.float16
+    else:
+        kp, vp = _c(k_pool, np.float16).copy(), _c(v_pool, np.float16).copy()
+    nb, hkv, bs, d = kp.shape
+    assert vp.shape == kp.shape
+    kn, vn = _c(k_new, np.float16), _c(v_new, np.float16)
+    bt = _c(block_tables, np.int32)
+    pos = _c(positions, np.int32).reshape(-1)
+    n = pos.size
+    assert kn.shape == (n, hkv, d) and vn.shape == kn.shape
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    assert bt.shape[0] == n or n == 0
+    flags = np.zeros(n, np.uint32)
+    written = np.full(n, -1, np.int32)
+    rc = lib.pkv_oracle_append(_ptr(kp), _ptr(vp), _ptr(kn), _ptr(vn), _ptr(bt), _ptr(pos),
+                               n, hkv, d, bs, mb, nb, _ptr(flags), _ptr(written))
+    if rc < 0:
+        raise ValueError("oracle rejected the append arguments")
+    return kp, vp, flags, written
+
+
+def append_int8(k_pool, v_pool, k_codes, v_codes, k_scales, v_scales, k_new, v_new,
+                block_tables, positions, *, inplace=False):
+    """Append into the fp16 pools, then re-quantize every written tile.
+
+    Returns (k_pool, v_pool, k_codes, v_codes, k_scales, v_scales, flags):
+    the fp16 pools after ``append_fp16`` and the INT8 pools in which the
+    (written block, every kv head) tiles are the ``quantize`` of the new fp16
+    tiles; all other tiles keep their codes and scales.
+    """
+    kp, vp, flags, written = append_fp16(k_pool, v_pool, k_new, v_new, block_tables,
+                                         positions, inplace=inplace)
+    ids = written[written >= 0]
+    if inplace:
+        quantize(kp, block_ids=ids, code_pool=k_codes, scales=k_scales, inplace=True)
+        quantize(vp, block_ids=ids, code_pool=v_codes, scales=v_scales, inplace=True)
+        kc, ks, vc, vs = k_codes, k_scales, v_codes, v_scales
+    else:
+        kc, ks = quantize(kp, block_ids=ids, code_pool=k_codes, scales=k_scales)
+        vc, vs = quantize(vp, block_ids=ids, code_pool=v_codes, scales=v_scales)
+    return kp, vp, kc, vc, ks, vs, flags
+
+
+EVICT_ALPHA = 0.7  # weights of the least-reference-count + age score
+EVICT_BETA = 0.3
+
+
+def evict_scores(refcnt, last_used, current_tick, alpha=EVICT_ALPHA, beta=EVICT_BETA):
+    """fp32 eviction score of every block; -inf for free (refcnt <= 0) blocks.
+
+    Returns (scores float32 [NB], number of candidate blocks).
+    """
+    lib = _load()
+    rc = _c(refcnt, np.int32).reshape(-1)
+    lu = _c(last_used, np.int64).reshape(-1)
+    assert rc.size == lu.size
+    scores = np.empty(rc.size, np.float32)
+    cand = lib.pkv_oracle_evict_scores(_ptr(scores), _ptr(rc), _ptr(lu), rc.size,
+                                       int(current_tick), float(alpha), float(beta))
+    return scores, int(cand)
+
+
+def evict_select(refcnt, last_used, current_tick, k, alpha=EVICT_ALPHA, beta=EVICT_BETA):
+    """The min(k, candidates) most evictable blocks, in ascending id order.
+
+    Returns (ids int32 [n], scores float32 [NB]).
+    """
+    lib = _load()
+    scores, _ = evict_scores(refcnt, last_used, current_tick, alpha, beta)
+    rc = _c(refcnt, np.int32).reshape(-1)
+    ids = np.empty(max(int(k), 0) + 1, np.int32)
+    n = lib.pkv_oracle_evict_select(_ptr(ids), _ptr(scores), _ptr(rc), rc.size, int(k))
+    if n < 0:
+        raise ValueError("oracle rejected the eviction arguments")
+    return ids[:n].copy(), scores

@@ -36,6 +36,26 @@
  *    design notes).  Computed in fp32 so that codes and scales can be
  *    compared bit for bit.
  *
+ *  - pkv_oracle_append: the write that precedes a decode step.  The new
+ *    token of sequence s sits at position t = positions[s]; its K and V rows
+ *    (one per kv head) go to slot t % B of physical block table[s][t / B]
+ *    -- the inverse of the decode gather ("PagedAttention & KV-Cache Memory
+ *    Management", section 2.1, and its prefill step that writes each token
+ *    at phys_block_id * B + token_offset; section 3.3.2 "append the delta
+ *    tokens").  Plain row copies of fp16 bit patterns, one sequence after
+ *    another.  The INT8 cache re-quantizes the written (block, kv-head) tiles
+ *    with pkv_oracle_quantize afterwards (done by the Python wrapper).
+ *
+ *  - pkv_oracle_evict_scores / pkv_oracle_evict_select: the
+ *    least-reference-count + age eviction score of "PagedAttention &
+ *    KV-Cache Memory Management", section 4.3.1,
+ *      score = alpha * (max_refcnt - refcnt) + beta * (current_tick - last_used),
+ *    evaluated in fp32 one rounding per operation, and the choice of the k
+ *    blocks to evict ("PagedKV-Fusion" README: scoring of every physical
+ *    block, then the eviction ids).  Blocks with refcnt <= 0 are free and are
+ *    not candidates; max_refcnt is the largest refcnt present.  A larger
+ *    score means more evictable; equal scores go to the smaller block id.
+ *
  * Conventions shared with the library (by specification, not by code):
  *   pools    [num_blocks][num_kv_heads][block_size][head_dim]
  *   scales   [num_blocks][num_kv_heads]
@@ -239,6 +259,143 @@ int64_t pkv_oracle_quantize(int8_t *code_pool, float *scales, const uint16_t *po
         }
     }
     return bad;
+}
+
+/*
+ * Append one token per sequence into fp16 pools (bit patterns).
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim]
+ *   positions     [num_seqs]: token index of the new token; < 0 = no token
+ *   flags         optional [num_seqs] output: ORACLE_BAD_CTX when the
+ *                 position is beyond max_blocks_per_seq * block_size,
+ *                 ORACLE_BAD_BLOCK when table[s][t / B] is not in
+ *                 [0, num_blocks); a flagged sequence writes nothing.
+ *   written_blocks optional [num_seqs] output: the physical block written,
+ *                 or -1.
+ * Returns the number of flagged sequences, or -1 on bad arguments.
+ */
+int64_t pkv_oracle_append(uint16_t *kpool, uint16_t *vpool, const uint16_t *k_new,
+                          const uint16_t *v_new, const int32_t *block_tables,
+                          const int32_t *positions, int num_seqs, int num_kv_heads,
+                          int head_dim, int block_size, int max_blocks_per_seq,
+                          int64_t num_blocks, uint32_t *flags, int32_t *written_blocks)
+{
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        max_blocks_per_seq < 0 || num_blocks < 0) {
+        return -1;
+    }
+    int64_t bad = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int64_t t = positions[s];
+        uint32_t flag = 0;
+        int64_t blk = -1;
+        if (t >= (int64_t)max_blocks_per_seq * block_size) {
+            flag = ORACLE_BAD_CTX;
+        } else if (t >= 0) {
+            blk = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+            if (blk < 0 || blk >= num_blocks) flag = ORACLE_BAD_BLOCK;
+        }
+        if (flags) flags[s] = flag;
+        if (flag) {
+            ++bad;
+            blk = -1;
+        }
+        if (written_blocks) written_blocks[s] = (int32_t)blk;
+        if (blk < 0) continue;
+        const int slot = (int)(t % block_size);
+        for (int kvh = 0; kvh < num_kv_heads; ++kvh) {
+            const int64_t dst = (((blk * num_kv_heads) + kvh) * block_size + slot) * head_dim;
+            const int64_t src = ((int64_t)s * num_kv_heads + kvh) * head_dim;
+            for (int i = 0; i < head_dim; ++i) {
+                kpool[dst + i] = k_new[src + i];
+                vpool[dst + i] = v_new[src + i];
+            }
+        }
+    }
+    return bad;
+}
+
+/*
+ * Eviction scores of num_blocks physical blocks, fp32, one rounding per
+ * operation (the file is built without FMA contraction):
+ *   d_ref = (float)(max_refcnt - refcnt[b])          exact int64 difference
+ *   d_age = (float)(current_tick - last_used[b])     exact int64 difference
+ *   score = alpha * d_ref + beta * d_age
+ * max_refcnt = the largest refcnt[b] (0 if none is positive).  Free blocks
+ * (refcnt <= 0) get -inf; a NaN score (inf - inf) is stored as -inf too.
+ * Returns the number of candidate (refcnt > 0) blocks.
+ */
+int64_t pkv_oracle_evict_scores(float *scores, const int32_t *refcnt, const int64_t *last_used,
+                                int64_t num_blocks, int64_t current_tick, float alpha,
+                                float beta)
+{
+    int32_t max_ref = 0;
+    int64_t candidates = 0;
+    for (int64_t b = 0; b < num_blocks; ++b) {
+        if (refcnt[b] > max_ref) max_ref = refcnt[b];
+        if (refcnt[b] > 0) ++candidates;
+    }
+    for (int64_t b = 0; b < num_blocks; ++b) {
+        if (refcnt[b] <= 0) {
+            scores[b] = -INFINITY;
+            continue;
+        }
+        const float d_ref = (float)((int64_t)max_ref - refcnt[b]);
+        const float d_age = (float)(current_tick - last_used[b]);
+        const float a = alpha * d_ref;
+        const float c = beta * d_age;
+        float sc = a + c;
+        if (isnan(sc)) sc = -INFINITY;
+        scores[b] = sc;
+    }
+    return candidates;
+}
+
+typedef struct {
+    float score;
+    int32_t id;
+} evict_entry;
+
+/* Descending score, then ascending block id. */
+static int evict_order(const void *pa, const void *pb)
+{
+    const evict_entry *a = (const evict_entry *)pa, *b = (const evict_entry *)pb;
+    if (a->score > b->score) return -1;
+    if (a->score < b->score) return 1;
+    return (a->id > b->id) - (a->id < b->id);
+}
+
+static int id_order(const void *pa, const void *pb)
+{
+    const int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a > b) - (a < b);
+}
+
+/*
+ * The k blocks to evict: sort the candidates (refcnt > 0) by score,
+ * largest first, equal scores by smaller id, keep the first min(k, count),
+ * and return them in ascending block-id order in evict_ids[0..n).
+ * Returns n, or -1 on bad arguments / allocation failure.
+ */
+int64_t pkv_oracle_evict_select(int32_t *evict_ids, const float *scores, const int32_t *refcnt,
+                                int64_t num_blocks, int64_t k)
+{
+    if (num_blocks < 0 || k < 0) return -1;
+    evict_entry *c = (evict_entry *)malloc(sizeof(evict_entry) * (size_t)(num_blocks + 1));
+    if (!c) return -1;
+    int64_t n = 0;
+    for (int64_t b = 0; b < num_blocks; ++b) {
+        if (refcnt[b] > 0) {
+            c[n].score = scores[b];
+            c[n].id = (int32_t)b;
+            ++n;
+        }
+    }
+    qsort(c, (size_t)n, sizeof(evict_entry), evict_order);
+    if (k < n) n = k;
+    for (int64_t j = 0; j < n; ++j) evict_ids[j] = c[j].id;
+    free(c);
+    qsort(evict_ids, (size_t)n, sizeof(int32_t), id_order);
+    return n;
 }
 
 /* Threads the OpenMP runtime will use for a parallel region (1 without OpenMP). */

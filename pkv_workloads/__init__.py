@@ -31,6 +31,10 @@ Configurations (sizes of the workloads this library is measured on):
   c5a_64x2048       64 x 2048, 32 q / 8 kv heads, d 128, 65536 blocks
   c5b_256_ragged    256 seqs, ctx ~ uniform integers [1, 4096], same heads and
                     pool
+
+``append_tokens`` draws the new K/V rows of an append step (N(0, 1) fp16);
+``eviction_state`` draws reference counts and last-use ticks of a block pool
+for eviction scoring.
 """
 from __future__ import annotations
 
@@ -190,6 +194,45 @@ def random_case(seed: int, *, num_seqs: int, num_heads: int, num_kv_heads: int,
                  head_dim=head_dim, num_blocks=max(need + extra_blocks, 1),
                  context_lens=ctx, seed=seed, nan_padding=nan_padding,
                  block_size=block_size)
+
+
+def append_tokens(w: DecodeWorkload, seed: int):
+    """New-token inputs for an append into ``w``'s pools.
+
+    Each sequence with context length c > 0 appends its token at position
+    c - 1 (so the table already holds the block, and a decode over c tokens
+    reads it); c == 0 gives position -1 (no token).  Returns (k_new, v_new
+    [N][Hkv][d] fp16 drawn N(0, 1), positions [N] int32).
+    """
+    n, hkv, d = w.num_seqs, w.num_kv_heads, w.head_dim
+    k_new = _normal_f16(_rng(seed, 6), (n, hkv, d))
+    v_new = _normal_f16(_rng(seed, 7), (n, hkv, d))
+    positions = (w.context_lens.astype(np.int64) - 1).astype(np.int32)
+    return k_new, v_new, positions
+
+
+@dataclasses.dataclass
+class EvictionState:
+    refcnt: np.ndarray      # [NB] int32; 0 = free block
+    last_used: np.ndarray   # [NB] int64 tick of the last decode step that read it
+    current_tick: int
+
+
+def eviction_state(num_blocks: int, seed: int, *, free_fraction: float = 0.1,
+                   current_tick: int = 100_000, max_age: int = 4096) -> EvictionState:
+    """Seeded block-manager state to score for eviction.
+
+    refcnt: 0 (free) with probability ``free_fraction``, else 1 + a
+    geometric(0.6) count capped at 16 (most blocks owned by one sequence, a
+    few shared prefixes); last_used: current_tick minus a uniform integer age
+    in [0, max_age].  Both are small integers, so equal scores are common.
+    """
+    rng = _rng(seed, 8)
+    ref = np.minimum(rng.geometric(0.6, size=num_blocks), 16).astype(np.int32)
+    ref[rng.random(num_blocks) < free_fraction] = 0
+    age = rng.integers(0, max_age, size=num_blocks, endpoint=True)
+    last = (current_tick - age).astype(np.int64)
+    return EvictionState(refcnt=ref, last_used=last, current_tick=int(current_tick))
 
 
 def shard_sequences(num_seqs: int, rank: int, world_size: int) -> range:
