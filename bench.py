@@ -10,8 +10,11 @@ Workload: 64 seqs x ctx 2048, 32 q / 8 kv heads, head_dim 128, block 16, a
 
 Metric: KV GB/s = algorithmic bytes per step / step time (the bytes of K, V
 and scales a step must read plus what the quantizer reads and writes), also
-sequence-steps/s and p50 us/step.  The fp16-KV decode of the same batch is
-timed alongside and reported under "variants".
+sequence-steps/s and p50 us/step.  The fp16-KV decode of the same batch, the
+token append that precedes a decode step (fp16, and INT8 with the fused tail
+re-quantize) and eviction scoring + choice of 15 % of the blocks at pools of
+1024, 16384 and 65536 blocks are timed alongside and reported under
+"variants".
 
 --impl reference times the CPU oracle (plain C, fp64 attention) on a bounded
 sample of the same workload, as the reference arm.
@@ -73,6 +76,24 @@ def decode_bytes(ctx, num_kv_heads, head_dim, elem_bytes, with_scales):
 def quantize_bytes(num_tiles, head_dim):
     """fp16 read + int8 written per value, one fp32 scale per tile (K and V)."""
     return num_tiles * 2 * (16 * head_dim * 3 + 4)
+
+
+def append_bytes(num_tiles, head_dim, int8):
+    """Per (sequence, kv head), K and V: the new fp16 row read and written;
+    INT8 adds the 15 other fp16 rows read, 16 rows of codes and a scale written."""
+    row = head_dim * 2
+    if not int8:
+        return num_tiles * 2 * 2 * row
+    return num_tiles * 2 * (16 * row + row + 16 * head_dim + 4)
+
+
+def evict_bytes(num_blocks, k):
+    """refcnt (4 B) and last_used (8 B) read, the fp32 score written per block,
+    k chosen ids and the count written."""
+    return num_blocks * (4 + 8 + 4) + 4 * k + 4
+
+
+EVICT_SIZES = (1024, 16384, 65536)  # the pages' pool sizes, then this workload's pool
 
 
 class ClockSampler:
@@ -251,7 +272,54 @@ def run_profile(args):
     for _ in range(args.warmup + args.steps):
         call()
     torch.cuda.synchronize()
-    print(f"profile run: {args.profile} decode x{args.warmup + args.steps}", flush=True)
+    print(f"profile run: {args.profile} x{args.warmup + args.steps}", flush=True)
+
+
+def run_profile_small(args):
+    """Append or eviction calls alone, for ncu: the append of the benchmark
+    batch's newest tokens (64 sequences, pool of 16384 blocks), or eviction
+    scoring of a 65536-block pool."""
+    import torch
+    import paged_kv_cache_234_gb300 as pkv
+    from paged_kv_cache_234_gb300 import build as pkv_build
+    pkv_build.build()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    if args.profile == "evict":
+        st = W.eviction_state(EVICT_SIZES[-1], 7)
+        ref, last = dev(st.refcnt), dev(st.last_used)
+        k = pkv.evict_count(ref.numel())
+        ids = torch.empty(k, dtype=torch.int32, device="cuda")
+        cnt = torch.empty(1, dtype=torch.int32, device="cuda")
+        sc = torch.empty(ref.numel(), dtype=torch.float32, device="cuda")
+        call = lambda: pkv.pkv_evict_select(ref, last, st.current_tick, k, ids, cnt, sc)
+    else:
+        w = W.build(CONFIG + "_pool16k", num_heads=32, num_kv_heads=8, head_dim=128,
+                    num_blocks=16384, context_lens=[2048] * 64, seed=1005)
+        kn, vn, pos = W.append_tokens(w, 99)
+        kf, vf = dev(w.k_pool), dev(w.v_pool)
+        kc = torch.zeros(w.k_pool.shape, dtype=torch.int8, device="cuda")
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros(w.k_pool.shape[:2], dtype=torch.float32, device="cuda")
+        vs = torch.zeros_like(ks)
+        a = (dev(kn), dev(vn), dev(w.block_tables), dev(pos))
+        call = lambda: pkv.pkv_append_int8(kf, vf, kc, vc, ks, vs, *a)
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    print(f"profile run: {args.profile} x{args.warmup + args.steps}", flush=True)
+
+
+def evict_cpu_us(num_blocks, reps=20):
+    """The oracle's eviction (scores + sort-based choice) on this host."""
+    import oracle
+    st = W.eviction_state(num_blocks, 7)
+    k = (num_blocks * 15) // 100
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.evict_select(st.refcnt, st.last_used, st.current_tick, k)
+        ts.append(time.perf_counter() - t0)
+    return 1e6 * statistics.median(ts)
 
 
 def main():
@@ -262,13 +330,17 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["int8", "fp16", "quantize"],
-                    help="profiling run: the same batch over a 16384-block pool, only "
-                         "warm-up + timed decode calls of one variant, no report line")
+    ap.add_argument("--profile", choices=["int8", "fp16", "quantize", "append", "evict"],
+                    help="profiling run: the same batch over a 16384-block pool (eviction: "
+                         "a 65536-block pool), only warm-up + timed calls of one kernel, "
+                         "no report line")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+        return
+    if args.profile in ("append", "evict"):
+        run_profile_small(args)
         return
     if args.profile:
         run_profile(args)
@@ -377,6 +449,35 @@ def main():
     f16_ms = timed(decode_fp16, Kd)
     q_ms = timed(step_int8, Kd)
 
+    # the write before a decode step: every sequence's newest token appended
+    # (fp16 rows; INT8 with the fused re-quantize of the tail tiles)
+    kn, vn, pos = W.append_tokens(w, 99)
+    app_args = (dev(kn), dev(vn), bt, dev(pos))
+    app16_ms = timed(lambda: pkv.pkv_append_fp16(kf, vf, *app_args, dev_status=status), Kd)
+    app8_ms = timed(lambda: pkv.pkv_append_int8(kf, vf, kc, vc, ks, vs, *app_args,
+                                                 dev_status=status), Kd)
+
+    # eviction scoring + choice of 15 % of the blocks, at the pages' pool sizes
+    evict = {}
+    for nb_e in EVICT_SIZES:
+        st_e = W.eviction_state(nb_e, 7)
+        ref_e, last_e = dev(st_e.refcnt), dev(st_e.last_used)
+        k_e = pkv.evict_count(nb_e)
+        ids_e = torch.empty(k_e, dtype=torch.int32, device="cuda")
+        cnt_e = torch.empty(1, dtype=torch.int32, device="cuda")
+        sc_e = torch.empty(nb_e, dtype=torch.float32, device="cuda")
+        fn_e = lambda: pkv.pkv_evict_select(ref_e, last_e, st_e.current_tick, k_e, ids_e,
+                                            cnt_e, sc_e)
+        for _ in range(args.warmup):
+            fn_e()
+        ms_e = timed(fn_e, Kd)
+        evict[str(nb_e)] = {"p50_us": 1e3 * statistics.median(ms_e),
+                            "p90_us": 1e3 * float(np.percentile(ms_e, 90)), "k": k_e,
+                            "GB/s": evict_bytes(nb_e, k_e) / (statistics.mean(ms_e) * 1e-3) / 1e9,
+                            "bytes": evict_bytes(nb_e, k_e)}
+        if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+            evict[str(nb_e)]["cpu_oracle_p50_us"] = evict_cpu_us(nb_e)
+
     # end to end through the public API with host buffers: per step the
     # query, block tables, context lengths and tail ids go host -> device and
     # the output comes back
@@ -447,6 +548,12 @@ def main():
             "quantize_tail_blocks": {"p50_us": 1e3 * statistics.median(q_ms),
                                      "tiles": 2 * ntiles,
                                      "bytes": quantize_bytes(ntiles, d)},
+            "append_fp16": {"p50_us": 1e3 * statistics.median(app16_ms), "rows": 2 * ntiles,
+                            "bytes": append_bytes(ntiles, d, False)},
+            "append_int8_fused_requantize": {"p50_us": 1e3 * statistics.median(app8_ms),
+                                             "tiles": 2 * ntiles,
+                                             "bytes": append_bytes(ntiles, d, True)},
+            "evict_select_15pct": evict,
         },
         "e2e": {"value": step_b * Ke / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},

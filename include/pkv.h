@@ -1,6 +1,9 @@
 /*
  * pkv.h -- C ABI of libpkv: decode-step paged attention over a
- * block-table-indexed KV cache, fp16 or INT8 KV, for NVIDIA GB300 (sm_103a).
+ * block-table-indexed KV cache, fp16 or INT8 KV, for NVIDIA GB300 (sm_103a),
+ * with the per-(block, kv head) INT8 quantizer, the token append that
+ * precedes a decode step, and eviction scoring with the choice of the blocks
+ * to evict.
  *
  * Sources for what each call computes:
  *  [PKF]  "PagedKV-Fusion" README (INT8 per-(block, head) quantized decode
@@ -12,7 +15,9 @@
  *         blocks) and 2 (block-table indirection, online softmax, FP32
  *         accumulation), 4 (GQA).
  *  [GLO]  "PagedAttention & KV-Cache Memory Management": section 2.1 (block
- *         table: block = table[t / B], slot = t % B).
+ *         table: block = table[t / B], slot = t % B; "Kernel Mechanics":
+ *         token writes), 3.3.2 (appending tokens), 4.3.1 (least-reference-
+ *         count + age eviction score).
  *
  * Layouts (all row-major, all pointers are DEVICE pointers owned by the
  * caller; the library never allocates, frees or synchronises):
@@ -194,6 +199,89 @@ PKV_API pkv_status pkv_paged_decode_int8_static_workspace(
     const int32_t *context_lens, int max_context_len, int num_seqs,
     int num_heads, int num_kv_heads, int head_dim, int block_size,
     float softmax_scale, int32_t *dev_status, void *stream);
+
+/*
+ * pkv_append_fp16 -- the KV write that precedes a decode step: for every
+ * sequence s with t = positions[s] >= 0, row t % 16 of tile
+ * (block_tables[s][t / 16], kv head h) of each pool is set to
+ * k_new[s][h][:] / v_new[s][h][:], for every kv head h
+ * ([GLO] section 2.1 "Logical Token Blocks & Page Tables": block = table[t /
+ * B], slot = t % B; "Kernel Mechanics": each token is written at
+ * phys_block_id * B + token_offset; section 3.3.2: "append the delta
+ * tokens").  A decode over context_lens[s] = t + 1 then attends to the new
+ * token.
+ *
+ *   k_cache, v_cache  fp16 pools [num_blocks][num_kv_heads][16][head_dim],
+ *                     written in place, 16-byte aligned
+ *   k_new, v_new      fp16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned
+ *   block_tables      int32 [num_seqs][max_blocks_per_seq] (may be NULL when
+ *                     max_blocks_per_seq is 0)
+ *   positions         int32 [num_seqs]: token index of the new token; a
+ *                     negative value means "no token for this sequence"
+ * A position >= max_blocks_per_seq * 16 sets PKV_DEV_BAD_CTX, a table entry
+ * outside [0, num_blocks) sets PKV_DEV_BAD_BLOCK; such a sequence writes
+ * nothing.  The caller guarantees that no two appended tokens of one call
+ * fall in the same physical block (a block shared by several sequences is
+ * copied before it is written); otherwise the result is undefined.
+ */
+PKV_API pkv_status pkv_append_fp16(void *k_cache, void *v_cache, int num_blocks,
+                                   const void *k_new, const void *v_new,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *positions, int num_seqs, int num_kv_heads,
+                                   int head_dim, int block_size, int32_t *dev_status,
+                                   void *stream);
+
+/*
+ * pkv_append_int8 -- pkv_append_fp16 for a cache kept as INT8 codes + scales
+ * next to its fp16 pools: the new rows are written to the fp16 pools, and
+ * every (block, kv head) tile that received a row is re-quantized into
+ * k_codes/v_codes and k_scales/v_scales, bit-identical to
+ * pkv_quantize_blocks on that block after the fp16 append (one fused kernel;
+ * [PKF] sequence diagram "INT8 survivors + scales").  All 16 slots of the
+ * tile are quantized, as pkv_quantize_blocks does.  Extra arguments:
+ *   k_codes, v_codes   int8 pools, 16-byte aligned
+ *   k_scales, v_scales fp32 [num_blocks][num_kv_heads], 4-byte aligned
+ */
+PKV_API pkv_status pkv_append_int8(void *k_cache, void *v_cache, int8_t *k_codes,
+                                   int8_t *v_codes, float *k_scales, float *v_scales,
+                                   int num_blocks, const void *k_new, const void *v_new,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *positions, int num_seqs, int num_kv_heads,
+                                   int head_dim, int block_size, int32_t *dev_status,
+                                   void *stream);
+
+/*
+ * pkv_evict_select -- score every physical block for eviction and choose
+ * the k most evictable ones, in one launch ([PKF] Overview component A
+ * "Eviction score: fused scoring + top-k over paged KV blocks", sequence
+ * diagram "score all physical blocks" -> "eviction ids").  The score is the
+ * least-reference-count + age heuristic of [GLO] section 4.3.1:
+ *   score[b] = alpha * (max_refcnt - refcnt[b]) + beta * (current_tick - last_used[b])
+ * evaluated in fp32, one rounding per operation, each difference formed
+ * exactly in integers and rounded to fp32; max_refcnt = max over b of
+ * refcnt[b].  A block with refcnt[b] <= 0 is free: it gets score -inf and is
+ * never chosen.  A NaN score (inf - inf with extreme weights) counts as -inf.
+ * The chosen blocks are the min(k, number of candidates) with the largest
+ * scores, equal scores going to the smaller block id; they are written to
+ * evict_ids[0 .. n) in ascending block-id order, n to *num_evicted, and -1
+ * to evict_ids[n .. k).  The [GLO] page gives alpha = 0.7, beta = 0.3.
+ *
+ *   refcnt       int32 [num_blocks], device; 4-byte aligned
+ *   last_used    int64 [num_blocks], device (ticks); 8-byte aligned
+ *   current_tick the present tick; every current_tick - last_used[b] must
+ *                fit in int64
+ *   alpha, beta  finite weights (else PKV_ERR_INVALID_ARG)
+ *   k            >= 0, blocks to choose
+ *   scores       optional fp32 [num_blocks] output (NULL: not written)
+ *   evict_ids    int32 [k] output (may be NULL when k == 0)
+ *   num_evicted  int32 device output
+ * num_blocks may be at most 16 * 49152 (786432) on a device that schedules
+ * 16-CTA clusters, else 8 * 49152; larger pools give PKV_ERR_UNSUPPORTED.
+ */
+PKV_API pkv_status pkv_evict_select(const int32_t *refcnt, const int64_t *last_used,
+                                    int num_blocks, int64_t current_tick, float alpha,
+                                    float beta, int k, float *scores, int32_t *evict_ids,
+                                    int32_t *num_evicted, void *stream);
 
 /*
  * Bytes of workspace a decode call with these sizes needs (either variant).

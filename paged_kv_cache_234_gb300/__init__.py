@@ -11,6 +11,9 @@ The functions carry the C names and take torch tensors:
 * ``pkv_quantize_blocks``     fp16 K/V tiles -> INT8 codes + fp32 scales
 * ``pkv_paged_decode_fp16``   decode-step attention over fp16 K/V pools
 * ``pkv_paged_decode_int8``   decode-step attention over INT8 K/V pools
+* ``pkv_append_fp16``         write one new token per sequence into fp16 pools
+* ``pkv_append_int8``         the same, re-quantizing every tile it writes
+* ``pkv_evict_select``        eviction scores of every block + the k to evict
 * ``pkv_decode_workspace_size``, ``pkv_set_decode_workers``,
   ``pkv_status_string``
 """
@@ -36,8 +39,13 @@ PKV_DEV_BAD_CTX = 2
 PKV_DEV_TIMEOUT = 4
 
 EXPORTED = ("pkv_quantize_blocks", "pkv_paged_decode_fp16", "pkv_paged_decode_int8",
-            "pkv_paged_decode_int8_static_workspace", "pkv_decode_workspace_size",
-            "pkv_set_decode_workers", "pkv_status_string")
+            "pkv_paged_decode_int8_static_workspace", "pkv_append_fp16", "pkv_append_int8",
+            "pkv_evict_select", "pkv_decode_workspace_size", "pkv_set_decode_workers",
+            "pkv_status_string")
+
+# weights of the least-reference-count + age eviction score
+EVICT_ALPHA = 0.7
+EVICT_BETA = 0.3
 
 # size of the scratch array behind pkv_paged_decode_int8_static_workspace
 PKV_STATIC_WORKSPACE_BYTES = 32 << 20
@@ -73,6 +81,13 @@ def lib() -> ctypes.CDLL:
         L.pkv_paged_decode_int8.argtypes = dec[:4] + [P, P] + dec[4:]
         L.pkv_paged_decode_int8_static_workspace.restype = I
         L.pkv_paged_decode_int8_static_workspace.argtypes = dec[:4] + [P, P] + dec[4:15] + dec[17:]
+        app = [P, P, I, P, P, P, I, P, I, I, I, I, P, P]
+        L.pkv_append_fp16.restype = I
+        L.pkv_append_fp16.argtypes = app
+        L.pkv_append_int8.restype = I
+        L.pkv_append_int8.argtypes = app[:2] + [P, P, P, P] + app[2:]
+        L.pkv_evict_select.restype = I
+        L.pkv_evict_select.argtypes = [P, P, I, ctypes.c_int64, F, F, I, P, P, P, P]
         L.pkv_decode_workspace_size.restype = Z
         L.pkv_decode_workspace_size.argtypes = [I, I, I, I, I]
         L.pkv_set_decode_workers.restype = I
@@ -224,3 +239,77 @@ def pkv_paged_decode_int8_static_workspace(out, query, k_codes, v_codes, k_scale
         float(softmax_scale), _ptr(dev_status), _stream(stream))
     if st != PKV_OK:
         raise PkvError(st, "pkv_paged_decode_int8_static_workspace")
+
+
+def _append(fn_name, k_cache, v_cache, codes, k_new, v_new, block_tables, positions,
+            dev_status, stream):
+    import torch
+    _check(k_cache, "k_cache", torch.float16)
+    _check(v_cache, "v_cache", torch.float16)
+    _check(k_new, "k_new", torch.float16)
+    _check(v_new, "v_new", torch.float16)
+    _check(block_tables, "block_tables", torch.int32)
+    _check(positions, "positions", torch.int32)
+    _check(dev_status, "dev_status", torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    n = positions.numel()
+    mb = block_tables.shape[1] if block_tables is not None and block_tables.dim() == 2 else 0
+    args = [_ptr(k_cache), _ptr(v_cache)]
+    if codes is not None:
+        kc, vc, ks, vs = codes
+        _check(kc, "k_codes", torch.int8)
+        _check(vc, "v_codes", torch.int8)
+        _check(ks, "k_scales", torch.float32)
+        _check(vs, "v_scales", torch.float32)
+        args += [_ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs)]
+    args += [nb, _ptr(k_new), _ptr(v_new), _ptr(block_tables), mb, _ptr(positions), n, hkv, d,
+             bs, _ptr(dev_status), _stream(stream)]
+    st = getattr(lib(), fn_name)(*args)
+    if st != PKV_OK:
+        raise PkvError(st, fn_name)
+
+
+def pkv_append_fp16(k_cache, v_cache, k_new, v_new, block_tables, positions, dev_status=None,
+                    stream=None) -> None:
+    """Write k_new/v_new [N][Hkv][d] at token positions[s] of each sequence
+    (slot positions[s] % 16 of block block_tables[s][positions[s] // 16])."""
+    _append("pkv_append_fp16", k_cache, v_cache, None, k_new, v_new, block_tables, positions,
+            dev_status, stream)
+
+
+def pkv_append_int8(k_cache, v_cache, k_codes, v_codes, k_scales, v_scales, k_new, v_new,
+                    block_tables, positions, dev_status=None, stream=None) -> None:
+    """pkv_append_fp16, then re-quantize every (block, kv head) tile written."""
+    _append("pkv_append_int8", k_cache, v_cache, (k_codes, v_codes, k_scales, v_scales), k_new,
+            v_new, block_tables, positions, dev_status, stream)
+
+
+def pkv_evict_select(refcnt, last_used, current_tick, k, evict_ids, num_evicted, scores=None,
+                     alpha=EVICT_ALPHA, beta=EVICT_BETA, stream=None) -> None:
+    """Score every block (refcnt int32 [NB], last_used int64 [NB]) and write
+    the min(k, candidates) most evictable ids, ascending, to evict_ids[:n]
+    (-1 after), n to num_evicted[0] and the fp32 scores to ``scores``."""
+    import torch
+    _check(refcnt, "refcnt", torch.int32)
+    _check(last_used, "last_used", torch.int64)
+    _check(evict_ids, "evict_ids", torch.int32)
+    _check(num_evicted, "num_evicted", torch.int32)
+    _check(scores, "scores", torch.float32)
+    nb = refcnt.numel()
+    if last_used.numel() != nb or (scores is not None and scores.numel() != nb):
+        raise ValueError("refcnt, last_used and scores must have one entry per block")
+    if evict_ids is not None and evict_ids.numel() < k:
+        raise ValueError("evict_ids must hold k entries")
+    st = lib().pkv_evict_select(_ptr(refcnt), _ptr(last_used), nb, int(current_tick),
+                                float(alpha), float(beta), int(k), _ptr(scores),
+                                _ptr(evict_ids), _ptr(num_evicted), _stream(stream))
+    if st != PKV_OK:
+        raise PkvError(st, "pkv_evict_select")
+
+
+def evict_count(num_blocks: int, percent: int = 15) -> int:
+    """Blocks to evict when a fixed percentage of the scored blocks goes:
+    floor(num_blocks * percent / 100) in integer arithmetic."""
+    if num_blocks < 0 or not 0 <= percent <= 100:
+        raise ValueError("bad block count or percentage")
+    return (int(num_blocks) * int(percent)) // 100

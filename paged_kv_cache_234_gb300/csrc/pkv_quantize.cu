@@ -15,36 +15,10 @@
 
 #include "pkv_host.cuh"
 #include "pkv_ptx.cuh"
+#include "pkv_quant.cuh"
 
 namespace pkv {
 namespace {
-
-constexpr int kQuantThreads = 128;  // one CTA per (block, kv head, K|V) tile
-
-// RNE(y) for |y| < 2^22 by the exact add of 1.5 * 2^23: the fp32 sum rounds
-// to nearest even at unit spacing; its low bits then hold the integer.
-constexpr float kRoundMagic = 12582912.0f;
-
-// code = round-half-even(fl32(x / scale)), clamped to [-127, 127]; a NaN
-// quotient gives 0.  y' = x * fl32(1/scale) is within 2 ulp of fl32(x/scale);
-// ulp <= 2^-17 for |x/scale| <= 127, so when y' is more than 2^-14 away from
-// every half-integer both round to the same integer.  Only quotients that
-// close to a tie (and NaN/inf cases) take the IEEE division.
-__device__ __forceinline__ int quant_code(float x, float scale, float rcp)
-{
-    const float yf = x * rcp;
-    const float t = yf + kRoundMagic;
-    const float r = t - kRoundMagic;
-    if (fabsf(yf - r) < 0.5f - 0.00006103515625f) {  // 0.5 - 2^-14; false for NaN/inf
-        return __float_as_int(t) - 0x4B400000;       // |r| <= 127: no clamp needed
-    }
-    const float y = __fdiv_rn(x, scale);
-    if (isnan(y)) return 0;  // 0/0, inf/inf or a NaN input
-    int c = __float2int_rn(y);
-    c = c > 127 ? 127 : c;
-    c = c < -127 ? -127 : c;
-    return c;
-}
 
 template <int kHeadDim>
 __global__ void __launch_bounds__(kQuantThreads)
@@ -61,7 +35,6 @@ __global__ void __launch_bounds__(kQuantThreads)
     // reads of the pools this kernel overwrites) are complete past this point
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int64_t task = blockIdx.x; task < 2 * tiles_per_pool; task += gridDim.x) {
         const bool is_v = task >= tiles_per_pool;
         const int64_t t = is_v ? task - tiles_per_pool : task;
@@ -82,44 +55,13 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) raw[c] = __ldcs(src + c * kQuantThreads + threadIdx.x);
 
-        float amax = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-            const __half2 *hp = reinterpret_cast<const __half2 *>(&raw[c]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __half22float2(hp[e]);
-                amax = fmaxf(amax, fabsf(f.x));  // fmaxf drops a NaN operand
-                amax = fmaxf(amax, fabsf(f.y));
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (lane == 0) warp_max[warp] = amax;
-        __syncthreads();
-#pragma unroll
-        for (int w = 0; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
-        __syncthreads();  // warp_max is reused by the next task
+        const float amax = cta_absmax(chunks_absmax(raw), warp_max);
         const float scale = __fdiv_rn(amax, 127.0f);
         const float rcp = __frcp_rn(scale);
 
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-            const __half2 *hp = reinterpret_cast<const __half2 *>(&raw[c]);
-            uint32_t packed[2];
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-                const float2 f0 = __half22float2(hp[2 * w]);
-                const float2 f1 = __half22float2(hp[2 * w + 1]);
-                const uint32_t b0 = static_cast<uint32_t>(quant_code(f0.x, scale, rcp)) & 0xffu;
-                const uint32_t b1 = static_cast<uint32_t>(quant_code(f0.y, scale, rcp)) & 0xffu;
-                const uint32_t b2 = static_cast<uint32_t>(quant_code(f1.x, scale, rcp)) & 0xffu;
-                const uint32_t b3 = static_cast<uint32_t>(quant_code(f1.y, scale, rcp)) & 0xffu;
-                packed[w] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            }
-            __stcs(dst + c * kQuantThreads + threadIdx.x, make_uint2(packed[0], packed[1]));
-        }
+        for (int c = 0; c < kChunks; ++c)
+            __stcs(dst + c * kQuantThreads + threadIdx.x, chunk_codes(raw[c], scale, rcp));
         if (threadIdx.x == 0) (is_v ? v_scales : k_scales)[tile] = scale;
     }
 }

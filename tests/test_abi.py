@@ -117,6 +117,59 @@ def test_quantize_host_validation(L):
     assert q(ids=FAKE, nids=0) == pkv.PKV_OK  # empty id list: nothing launched
 
 
+def test_append_host_validation(L):
+    def a(int8=False, **kw):
+        x = dict(k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE, nb=16, kn=FAKE, vn=FAKE,
+                 tables=FAKE, mb=4, pos=FAKE, n=2, hkv=2, d=64, bs=16, status=None, stream=None)
+        x.update(kw)
+        head = [x["k"], x["v"]]
+        if int8:
+            head += [x["kc"], x["vc"], x["ks"], x["vs"]]
+        args = head + [x["nb"], x["kn"], x["vn"], x["tables"], x["mb"], x["pos"], x["n"],
+                       x["hkv"], x["d"], x["bs"], x["status"], x["stream"]]
+        return (L.pkv_append_int8 if int8 else L.pkv_append_fp16)(*args)
+    for int8 in (False, True):
+        assert a(int8, k=None) == pkv.PKV_ERR_INVALID_ARG
+        assert a(int8, pos=None) == pkv.PKV_ERR_INVALID_ARG
+        assert a(int8, tables=None) == pkv.PKV_ERR_INVALID_ARG
+        assert a(int8, nb=0) == pkv.PKV_ERR_INVALID_ARG
+        assert a(int8, n=-1) == pkv.PKV_ERR_INVALID_ARG
+        assert a(int8, d=96) == pkv.PKV_ERR_UNSUPPORTED
+        assert a(int8, bs=8) == pkv.PKV_ERR_UNSUPPORTED
+        assert a(int8, kn=FAKE + 8) == pkv.PKV_ERR_MISALIGNED
+        assert a(int8, pos=FAKE + 2) == pkv.PKV_ERR_MISALIGNED
+        assert a(int8, n=0) == pkv.PKV_OK  # nothing launched
+    assert a(True, ks=None) == pkv.PKV_ERR_INVALID_ARG
+    assert a(True, vc=FAKE + 4) == pkv.PKV_ERR_MISALIGNED
+
+
+def test_evict_host_validation(L):
+    def e(**kw):
+        x = dict(ref=FAKE, last=FAKE, nb=1024, tick=10, alpha=0.7, beta=0.3, k=5, scores=None,
+                 ids=FAKE, count=FAKE, stream=None)
+        x.update(kw)
+        return L.pkv_evict_select(x["ref"], x["last"], x["nb"], x["tick"], x["alpha"],
+                                  x["beta"], x["k"], x["scores"], x["ids"], x["count"],
+                                  x["stream"])
+    assert e(k=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert e(nb=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert e(count=None) == pkv.PKV_ERR_INVALID_ARG
+    assert e(ref=None) == pkv.PKV_ERR_INVALID_ARG
+    assert e(ids=None) == pkv.PKV_ERR_INVALID_ARG
+    assert e(alpha=float("nan")) == pkv.PKV_ERR_INVALID_ARG
+    assert e(beta=float("inf")) == pkv.PKV_ERR_INVALID_ARG
+    assert e(last=FAKE + 4) == pkv.PKV_ERR_MISALIGNED
+    assert e(scores=FAKE + 2) == pkv.PKV_ERR_MISALIGNED
+
+
+# The PagedKV-Fusion README's end-to-end demos evict 15 % of the scored
+# blocks: 173 of 1155 (CPU reference) and 85 of 568 (CUDA run).
+def test_evict_count_matches_the_pages_examples():
+    assert pkv.evict_count(1155) == 173
+    assert pkv.evict_count(568) == 85
+    assert pkv.evict_count(0) == 0 and pkv.evict_count(100, 100) == 100
+
+
 def test_set_decode_workers_rejects_negative(L):
     assert L.pkv_set_decode_workers(-1) == pkv.PKV_ERR_INVALID_ARG
     assert L.pkv_set_decode_workers(0) == pkv.PKV_OK
