@@ -11,16 +11,21 @@
 // ids").  Blocks with refcnt <= 0 are free and are never chosen; max_refcnt is
 // the largest refcnt of the pool; equal scores go to the smaller block id.
 //
-// GB300 design: one thread-block cluster (up to 16 CTAs of 1024 threads) owns
-// the whole pool; each CTA keeps its slice of 32-bit order keys in shared
-// memory, so the pool is read from HBM once.  The k-th largest key is found by
-// a four-pass MSB radix select (8-bit digits): every CTA counts its slice into
-// a shared-memory histogram (warp-aggregated atomics), one cluster barrier,
-// then every CTA sums the cluster's histograms through distributed shared
-// memory and picks the same digit.  A final CTA scan plus one more exchange of
-// per-CTA counts places the chosen ids, in ascending block-id order.  No
-// global atomics, no second launch, no spin-waits: the cluster barrier is the
-// hardware's and every CTA of a cluster is resident together.
+// GB300 design: one thread-block cluster (up to 16 CTAs of 512 threads) owns
+// the whole pool; each CTA copies its slice of reference counts and ages into
+// shared memory with 16-byte cp.async (all copies in flight at once) and keeps
+// its 32-bit order keys there, so the pool is read from HBM once.  The k-th
+// largest key is found by a four-pass MSB radix select (8-bit digits): every
+// CTA counts its slice into a local histogram (warp-aggregated shared-memory
+// atomics), then adds its nonzero bins into every CTA's merged histogram with
+// red.shared::cluster through distributed shared memory; after one cluster
+// barrier each CTA scans the merged counts in its own shared memory and picks
+// the same digit.  The chosen ids are placed in ascending block-id order by a
+// CTA scan plus one more exchange of per-CTA counts.  Data only ever moves by
+// pushes into peers before a barrier, so no CTA reads a peer after the last
+// barrier and CTAs leave independently.  No global atomics, no second launch,
+// no spin-waits (the barriers are the hardware's; a cluster's CTAs are resident
+// together); a one-CTA cluster uses plain CTA barriers.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -33,11 +38,20 @@
 namespace pkv {
 namespace {
 
-constexpr int kEvThreads = 1024;
+// Block shape and cluster sizing; the defaults are the measured best on GB300.
+#ifndef PKV_EVICT_THREADS
+#define PKV_EVICT_THREADS 512
+#endif
+#ifndef PKV_EVICT_SLICE
+#define PKV_EVICT_SLICE 2048
+#endif
+constexpr int kEvThreads = PKV_EVICT_THREADS;
 constexpr int kEvWarps = kEvThreads / 32;
-constexpr int kEvBins = 256;
+constexpr int kEvBins = 256;          // 8-bit digits: four passes from the top byte
+constexpr int kEvMaxCluster = 16;
 constexpr int kEvMaxSlice = 49152;    // keys per CTA in shared memory (192 KiB)
-constexpr int kEvTargetSlice = 4096;  // keys per CTA that sets the cluster size
+constexpr int kEvStageSlice = 16384;  // slices up to this also stage the ages (12 B per block)
+constexpr int kEvTargetSlice = PKV_EVICT_SLICE;  // keys per CTA that sets the cluster size
 constexpr uint32_t kNoBin = 0xffffffffu;
 
 struct EvictParams {
@@ -49,8 +63,10 @@ struct EvictParams {
     long long tick;
     float alpha, beta;
     int num_blocks;
-    int slice;  // blocks per CTA
+    int slice;   // blocks per CTA, a multiple of 4
     int k;
+    int staged;  // 1: refcnt and last_used are copied to shared memory with
+                 // 16-byte cp.async (16-byte aligned inputs, slice <= kEvStageSlice)
 };
 
 // Order-preserving map of a (non-NaN) fp32 score to a uint32; -0 maps with
@@ -62,42 +78,54 @@ __device__ __forceinline__ uint32_t score_key(float s)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Inclusive scan of one value per thread in thread order; *total gets the
-// CTA sum.  warp_sums: kEvWarps words of shared memory.
-__device__ __forceinline__ uint32_t cta_scan(uint32_t v, uint32_t *warp_sums, uint32_t *total)
+// Barrier over the CTAs that exchange data: the whole cluster (release /
+// acquire, so shared-memory writes into peers before it are visible after
+// it), or just this CTA when the cluster has one.
+__device__ __forceinline__ void group_sync(uint32_t csize)
+{
+    if (csize > 1)
+        ptx::cluster_sync();
+    else
+        __syncthreads();
+}
+
+// Exclusive scan, over the first 256 threads (8 warps), of one value each,
+// top bin first; the others pass 0.  *total gets the sum.  part: 8 words.
+__device__ __forceinline__ uint32_t bins_exclusive_scan(uint32_t v, uint32_t *part,
+                                                        uint32_t *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
+        const uint32_t n = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += n;
     }
-    if (lane == 31) warp_sums[warp] = v;
+    if (lane == 31 && warp < kEvBins / 32) part[warp] = x;
     __syncthreads();
-    if (warp == 0) {
-        uint32_t w = warp_sums[lane];
+    uint32_t before = 0, sum = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t n = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += n;
-        }
-        warp_sums[lane] = w;
+    for (int w = 0; w < kEvBins / 32; ++w) {
+        const uint32_t pw = part[w];
+        before += w < warp ? pw : 0u;
+        sum += pw;
     }
-    __syncthreads();
-    const uint32_t before = warp ? warp_sums[warp - 1] : 0u;
-    *total = warp_sums[kEvWarps - 1];
-    __syncthreads();  // warp_sums is reused by the next scan
-    return v + before;
+    *total = sum;
+    return before + x - v;
 }
 
 __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
 {
-    extern __shared__ uint32_t keys[];  // this CTA's slice
-    __shared__ uint32_t hist[2][kEvBins];
-    __shared__ uint32_t warp_sums[kEvWarps];
-    __shared__ uint32_t x_ref[2];  // this CTA's max refcnt and candidate count
-    __shared__ uint32_t x_sel;     // this CTA's (eq << 16 | gt) selection counts
-    __shared__ uint32_t bcast[4];
+    extern __shared__ __align__(16) unsigned char ev_smem[];
+    uint32_t *keys = reinterpret_cast<uint32_t *>(ev_smem);  // this CTA's slice
+    long long *ages = reinterpret_cast<long long *>(ev_smem + 4 * p.slice);  // when staged
+    __shared__ uint32_t warp_hist[kEvWarps][kEvBins];  // each warp's counts of one pass
+    __shared__ uint32_t merged[2][kEvBins];      // the cluster's counts, alternate passes
+    __shared__ uint32_t peer_ref[kEvMaxCluster][2];  // every CTA's max refcnt, candidates
+    __shared__ uint32_t peer_sel[kEvMaxCluster];     // every CTA's (eq << 16 | gt) counts
+    __shared__ uint32_t warp_a[kEvWarps], warp_b[kEvWarps];
+    __shared__ uint32_t part[kEvBins / 32];
+    __shared__ uint32_t bcast[2];
 
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
@@ -106,13 +134,37 @@ __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
     const int64_t lo = static_cast<int64_t>(rank) * p.slice;
     const int64_t left = static_cast<int64_t>(p.num_blocks) - lo;
     const int n_local = static_cast<int>(left < 0 ? 0 : (left < p.slice ? left : p.slice));
+    const long long *last_used = reinterpret_cast<const long long *>(p.last_used) + lo;
+    for (int b = tid; b < kEvWarps * kEvBins; b += kEvThreads) (&warp_hist[0][0])[b] = 0;
+    if (tid < kEvBins) {
+        merged[0][tid] = 0;  // peers add into it only after the first group barrier
+        merged[1][tid] = 0;
+    }
 
-    // 1. reference counts: max and candidates over the pool
+    // 1. reference counts (max and candidates over the pool).  Staged: both
+    // input slices are copied to shared memory at once (all copies in
+    // flight together), so the ages cost no second round trip to DRAM.
+    const int32_t *refcnt = p.refcnt + lo;
+    if (p.staged) {
+        const int nr = n_local >> 2, na = n_local >> 1;  // 16-byte chunks
+        for (int c = tid; c < nr; c += kEvThreads)
+            ptx::cp_async_16(ptx::smem_addr(keys + 4 * c), refcnt + 4 * c);
+        for (int c = tid; c < na; c += kEvThreads)
+            ptx::cp_async_16(ptx::smem_addr(ages + 2 * c), last_used + 2 * c);
+        if (tid == 0) {
+            for (int j = 4 * nr; j < n_local; ++j) keys[j] = static_cast<uint32_t>(__ldg(refcnt + j));
+            for (int j = 2 * na; j < n_local; ++j) ages[j] = __ldg(last_used + j);
+        }
+        ptx::cp_async_wait_all();
+    } else {
+#pragma unroll 4
+        for (int j = tid; j < n_local; j += kEvThreads) keys[j] = static_cast<uint32_t>(__ldg(refcnt + j));
+    }
+    __syncthreads();
     int32_t rmax = 0;
     uint32_t cand = 0;
     for (int j = tid; j < n_local; j += kEvThreads) {
-        const int32_t r = __ldg(p.refcnt + lo + j);
-        keys[j] = static_cast<uint32_t>(r);
+        const int32_t r = static_cast<int32_t>(keys[j]);
         rmax = max(rmax, r);
         cand += r > 0;
     }
@@ -122,49 +174,38 @@ __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
         cand += __shfl_xor_sync(0xffffffffu, cand, o);
     }
     if (lane == 0) {
-        hist[0][warp] = static_cast<uint32_t>(rmax);
-        hist[1][warp] = cand;
+        warp_a[warp] = static_cast<uint32_t>(rmax);
+        warp_b[warp] = cand;
     }
     __syncthreads();
     if (warp == 0) {
-        int32_t m = static_cast<int32_t>(hist[0][lane]);
-        uint32_t c = hist[1][lane];
+        int32_t m = lane < kEvWarps ? static_cast<int32_t>(warp_a[lane]) : 0;
+        uint32_t c = lane < kEvWarps ? warp_b[lane] : 0u;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
             c += __shfl_xor_sync(0xffffffffu, c, o);
         }
-        if (lane == 0) {
-            x_ref[0] = static_cast<uint32_t>(m);
-            x_ref[1] = c;
-        }
-    }
-    ptx::cluster_sync();
-    if (warp == 0) {
-        int32_t m = 0;
-        uint32_t c = 0;
+        // push this CTA's figures into slot `rank` of every CTA of the cluster
         if (static_cast<uint32_t>(lane) < csize) {
-            m = static_cast<int32_t>(ptx::ld_cluster_u32(ptx::smem_addr(&x_ref[0]), lane));
-            c = ptx::ld_cluster_u32(ptx::smem_addr(&x_ref[1]), lane);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-            c += __shfl_xor_sync(0xffffffffu, c, o);
-        }
-        if (lane == 0) {
-            bcast[0] = static_cast<uint32_t>(m);
-            bcast[1] = c;
+            ptx::st_cluster_addr(ptx::map_cluster(ptx::smem_addr(&peer_ref[rank][0]), lane),
+                                 static_cast<uint32_t>(m));
+            ptx::st_cluster_addr(ptx::map_cluster(ptx::smem_addr(&peer_ref[rank][1]), lane), c);
         }
     }
-    __syncthreads();
-    const int32_t max_ref = static_cast<int32_t>(bcast[0]);
-    const uint32_t n_cand = bcast[1];
+    group_sync(csize);
+    int32_t max_ref = 0;
+    uint32_t n_cand = 0;
+    for (uint32_t c = 0; c < csize; ++c) {
+        max_ref = max(max_ref, static_cast<int32_t>(peer_ref[c][0]));
+        n_cand += peer_ref[c][1];
+    }
 
     // 2. scores (written out) and order keys (kept in shared memory)
+#pragma unroll 4
     for (int j = tid; j < n_local; j += kEvThreads) {
+        const long long used = p.staged ? ages[j] : __ldg(last_used + j);
         const int32_t r = static_cast<int32_t>(keys[j]);
-        const long long used = __ldg(reinterpret_cast<const long long *>(p.last_used) + lo + j);
         float sc = -INFINITY;
         uint32_t key = 0;
         if (r > 0) {
@@ -189,13 +230,15 @@ __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
         thresh = 0;            // every candidate
         kk = 0;
     } else {
+        // MSB radix select of the k-th largest key, one byte per pass.  Each
+        // CTA counts its slice locally, then adds its nonzero bins into the
+        // merged histogram of every CTA of the cluster; one group barrier,
+        // and every CTA holds the cluster's counts in its own shared memory.
         uint32_t prefix = 0, mask = 0;
         kk = k;
+#pragma unroll 1
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
-            uint32_t *h = hist[pass & 1];
-            if (tid < kEvBins) h[tid] = 0;
-            __syncthreads();
             for (int j0 = 0; j0 < n_local; j0 += kEvThreads) {
                 const int j = j0 + tid;
                 uint32_t bin = kNoBin;
@@ -204,78 +247,94 @@ __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
                     if (key != 0 && (key & mask) == prefix) bin = (key >> shift) & 0xffu;
                 }
                 const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-                if (bin != kNoBin && lane == __ffs(peers) - 1) atomicAdd(&h[bin], __popc(peers));
+                if (bin != kNoBin && lane == __ffs(peers) - 1)
+                    warp_hist[warp][bin] += __popc(peers);  // this warp's own row
             }
-            // every CTA's histogram of this pass is complete past the barrier;
-            // the other buffer is the one the next pass clears, and all reads
-            // of it (two passes back) finished before this barrier
-            ptx::cluster_sync();
-            uint32_t cnt = 0;
+            __syncthreads();
+            uint32_t *m = merged[pass & 1];
             if (tid < kEvBins) {
-                const uint32_t addr = ptx::smem_addr(&h[kEvBins - 1 - tid]);  // top bin first
-                for (uint32_t c = 0; c < csize; ++c) cnt += ptx::ld_cluster_u32(addr, c);
+                uint32_t v = 0;
+#pragma unroll
+                for (int w = 0; w < kEvWarps; ++w) {
+                    v += warp_hist[w][tid];
+                    warp_hist[w][tid] = 0;
+                }
+                if (v) {
+                    const uint32_t addr = ptx::smem_addr(&m[tid]);
+                    for (uint32_t c = 0; c < csize; ++c)
+                        ptx::red_add_cluster(ptx::map_cluster(addr, c), v);
+                }
+                // the other buffer was read in the previous pass (before the
+                // barrier below, in every CTA): clear it for the next pass
+                merged[(pass + 1) & 1][tid] = 0;
             }
+            group_sync(csize);
+            const uint32_t cnt = tid < kEvBins ? m[kEvBins - 1 - tid] : 0u;  // top bin first
             uint32_t total;
-            const uint32_t incl = cta_scan(cnt, warp_sums, &total);
-            if (tid < kEvBins && incl - cnt < kk && kk <= incl) {
-                bcast[2] = kEvBins - 1 - tid;
-                bcast[3] = incl - cnt;  // keys in higher bins
+            const uint32_t above = bins_exclusive_scan(cnt, part, &total);
+            if (tid < kEvBins && above < kk && kk <= above + cnt) {
+                bcast[0] = kEvBins - 1 - tid;
+                bcast[1] = above;  // keys in higher bins
             }
             __syncthreads();
-            prefix |= bcast[2] << shift;
+            prefix |= bcast[0] << shift;
             mask |= 0xffu << shift;
-            kk -= bcast[3];
-            __syncthreads();
+            kk -= bcast[1];
         }
         thresh = prefix;
     }
 
-    // 4. place the chosen ids in ascending block-id order: each thread owns a
-    // contiguous run of the slice; counts are < 2^16 per CTA, packed in one word
-    const int per = (n_local + kEvThreads - 1) / kEvThreads;
-    const int j0 = min(tid * per, n_local), j1 = min(j0 + per, n_local);
-    uint32_t gt = 0, eq = 0;
-    for (int j = j0; j < j1; ++j) {
-        const uint32_t key = keys[j];
-        gt += key > thresh;
-        eq += key == thresh;
+    // 4. place the chosen ids in ascending block-id order.  Each warp owns a
+    // contiguous segment of the slice and walks it in 32-key chunks (lane l
+    // reads key base + l: no bank conflicts); ballots give each key's rank.
+    const int seg = ((n_local + kEvWarps * 32 - 1) / (kEvWarps * 32)) * 32;
+    const int s0 = min(warp * seg, n_local), s1 = min(s0 + seg, n_local);
+    uint32_t gt = 0, eq = 0;  // warp-uniform counts over the segment
+    for (int base = s0; base < s1; base += 32) {
+        const int j = base + lane;
+        const uint32_t key = j < s1 ? keys[j] : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, j < s1 && key > thresh));
+        eq += __popc(__ballot_sync(0xffffffffu, j < s1 && key == thresh));
     }
-    const uint32_t mine = gt | (eq << 16);
-    uint32_t cta_total;
-    const uint32_t before = cta_scan(mine, warp_sums, &cta_total) - mine;
-    if (tid == 0) x_sel = cta_total;
-    ptx::cluster_sync();
-    if (warp == 0) {
-        uint32_t g = 0, e = 0;
-        if (static_cast<uint32_t>(lane) < rank) {
-            const uint32_t v = ptx::ld_cluster_u32(ptx::smem_addr(&x_sel), lane);
-            g = v & 0xffffu;
-            e = v >> 16;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            g += __shfl_xor_sync(0xffffffffu, g, o);
-            e += __shfl_xor_sync(0xffffffffu, e, o);
-        }
-        if (lane == 0) {
-            bcast[0] = g;
-            bcast[1] = e;
-        }
+    if (lane == 0) {
+        warp_a[warp] = gt;
+        warp_b[warp] = eq;
     }
     __syncthreads();
-    uint32_t gt_b = bcast[0] + (before & 0xffffu), eq_b = bcast[1] + (before >> 16);
-    for (int j = j0; j < j1; ++j) {
-        const uint32_t key = keys[j];
-        // an output slot is below k by construction; the check keeps every
+    uint32_t gt_b = 0, eq_b = 0, cta_gt = 0, cta_eq = 0;
+    for (int w = 0; w < kEvWarps; ++w) {
+        gt_b += w < warp ? warp_a[w] : 0u;
+        eq_b += w < warp ? warp_b[w] : 0u;
+        cta_gt += warp_a[w];
+        cta_eq += warp_b[w];
+    }
+    if (tid < static_cast<int>(csize))
+        ptx::st_cluster_addr(ptx::map_cluster(ptx::smem_addr(&peer_sel[rank]), tid),
+                             cta_gt | (cta_eq << 16));
+    // after this barrier no CTA touches another's shared memory: CTAs may
+    // leave in any order
+    group_sync(csize);
+    for (uint32_t c = 0; c < rank; ++c) {
+        gt_b += peer_sel[c] & 0xffffu;
+        eq_b += peer_sel[c] >> 16;
+    }
+    const uint32_t below = (1u << lane) - 1u;  // lanes before this one
+    for (int base = s0; base < s1; base += 32) {
+        const int j = base + lane;
+        const uint32_t key = j < s1 ? keys[j] : 0u;
+        const uint32_t gm = __ballot_sync(0xffffffffu, j < s1 && key > thresh);
+        const uint32_t em = __ballot_sync(0xffffffffu, j < s1 && key == thresh);
+        const uint32_t g = gt_b + __popc(gm & below), e = eq_b + __popc(em & below);
+        // an output slot is below k by construction; the checks keep every
         // store inside the caller's k-entry buffer regardless
-        if (key > thresh) {
-            const uint32_t at = gt_b + min(eq_b, kk);
+        if (j < s1 && key > thresh) {
+            const uint32_t at = g + min(e, kk);
             if (at < k) p.ids[at] = static_cast<int32_t>(lo + j);
-            ++gt_b;
-        } else if (key == thresh) {
-            if (eq_b < kk && gt_b + eq_b < k) p.ids[gt_b + eq_b] = static_cast<int32_t>(lo + j);
-            ++eq_b;
+        } else if (j < s1 && key == thresh && e < kk && g + e < k) {
+            p.ids[g + e] = static_cast<int32_t>(lo + j);
         }
+        gt_b += __popc(gm);
+        eq_b += __popc(em);
     }
 
     // 5. the count, and -1 in the unused tail of the id buffer
@@ -284,7 +343,6 @@ __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
     for (int64_t i = n_sel + static_cast<int64_t>(rank) * kEvThreads + tid; i < p.k;
          i += static_cast<int64_t>(csize) * kEvThreads)
         p.ids[i] = -1;
-    ptx::cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
 // One-time set-up per device: allow the full shared-memory slice, and find
@@ -349,9 +407,12 @@ extern "C" pkv_status pkv_evict_select(const int32_t *refcnt, const int64_t *las
     int64_t csize = (static_cast<int64_t>(num_blocks) + kEvTargetSlice - 1) / kEvTargetSlice;
     if (csize < 1) csize = 1;
     if (csize > cmax) csize = cmax;
-    const int64_t slice = (static_cast<int64_t>(num_blocks) + csize - 1) / csize;
+    int64_t slice = (static_cast<int64_t>(num_blocks) + csize - 1) / csize;
+    slice = (slice + 3) & ~static_cast<int64_t>(3);
     if (slice > kEvMaxSlice) return PKV_ERR_UNSUPPORTED;
-    const size_t smem = static_cast<size_t>(slice > 0 ? slice : 1) * sizeof(uint32_t);
+    const bool staged = num_blocks > 0 && slice <= kEvStageSlice && aligned(refcnt, 16) &&
+                        aligned(last_used, 16);
+    const size_t smem = static_cast<size_t>(slice > 0 ? slice : 4) * (staged ? 12 : 4);
     EvictParams prm;
     prm.refcnt = refcnt;
     prm.last_used = last_used;
@@ -364,6 +425,7 @@ extern "C" pkv_status pkv_evict_select(const int32_t *refcnt, const int64_t *las
     prm.num_blocks = num_blocks;
     prm.slice = static_cast<int>(slice);
     prm.k = k;
+    prm.staged = staged ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(csize));
     cfg.blockDim = dim3(kEvThreads);

@@ -105,6 +105,18 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte
+// aligned), cached in L2 only, and the wait for all of this thread's copies.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Arrive on bar once every cp.async this thread issued so far has landed.
 // .noinc: the arrival counts against the count given at mbarrier.init.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
@@ -220,6 +232,32 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t local, uint32_t rank
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
     return v;
+}
+
+// Address in CTA `rank`'s shared memory of the word at `local` in this CTA
+// (a shared::cluster address), and plain accesses through such addresses.
+__device__ __forceinline__ uint32_t map_cluster(uint32_t local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    return remote;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_addr(uint32_t cluster_addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_cluster_addr(uint32_t cluster_addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_cluster(uint32_t cluster_addr, uint32_t v)
+{
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 }  // namespace ptx
