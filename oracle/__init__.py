@@ -31,7 +31,14 @@ Every function cites the passage it follows:
   blocks (PagedKV-Fusion README: score every physical block, return the
   eviction ids).
 
-All functions here are pinned by tests in ``tests/test_oracle_pins.py``.
+* ``block_manager.BlockManagerModel`` -- the block manager (free list,
+  reference counts, prefix sharing, copy-on-write, fragmentation figures) of
+  the "paged-attention-runtime" summary (CORE CAPABILITIES 1) and of
+  "PagedAttention & KV-Cache Memory Management" (the prefix-sharing allocator,
+  section 4.1.1), as a plain Python model.
+
+All functions here are pinned by tests in ``tests/test_oracle_pins.py``,
+``tests/test_oracle_append_evict.py`` and ``tests/test_oracle_block_manager.py``.
 """
 from __future__ import annotations
 
