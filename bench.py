@@ -12,9 +12,10 @@ Metric: KV GB/s = algorithmic bytes per step / step time (the bytes of K, V
 and scales a step must read plus what the quantizer reads and writes), also
 sequence-steps/s and p50 us/step.  The fp16-KV decode of the same batch, the
 token append that precedes a decode step (fp16, and INT8 with the fused tail
-re-quantize) and eviction scoring + choice of 15 % of the blocks at pools of
-1024, 16384 and 65536 blocks are timed alongside and reported under
-"variants".
+re-quantize), eviction scoring + choice of 15 % of the blocks at pools of
+1024, 16384 and 65536 blocks, the copy-on-write block copies (64 and 4096
+blocks of K and V) and the host block manager's throughput are timed
+alongside and reported under "variants".
 
 --impl reference times the CPU oracle (plain C, fp64 attention) on a bounded
 sample of the same workload, as the reference arm.
@@ -94,6 +95,33 @@ def evict_bytes(num_blocks, k):
 
 
 EVICT_SIZES = (1024, 16384, 65536)  # the pages' pool sizes, then this workload's pool
+COPY_PAIRS = (64, 4096)  # copy-on-write batches: one decode step's tails, a large fork
+
+
+def block_manager_rate(num_blocks=65536, batch=128, seconds=1.0, model=False):
+    """Blocks per second through allocate + copy-on-write + free cycles of
+    `batch`-block requests (each block also forked once, so every
+    copy-on-write copies) on the native manager, or on the oracle's model."""
+    ids_per_cycle = 0
+    if model:
+        from oracle.block_manager import BlockManagerModel
+        bm = BlockManagerModel(num_blocks)
+        alloc = lambda: bm.allocate([0] * batch)
+        fork, cow, free = bm.fork, bm.cow_batch, bm.free
+    else:
+        import paged_kv_cache_234_gb300 as pkv
+        bm = pkv.BlockManager(num_blocks)
+        alloc = lambda: bm.allocate(batch)
+        fork, cow, free = bm.fork, (lambda ids: bm.cow(ids)), bm.free
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        a = alloc()
+        fork(a)
+        new, _ = cow(a)
+        free(a)
+        free(new)
+        ids_per_cycle += batch
+    return ids_per_cycle / (time.perf_counter() - t0)
 
 
 class ClockSampler:
@@ -457,6 +485,26 @@ def main():
     app8_ms = timed(lambda: pkv.pkv_append_int8(kf, vf, kc, vc, ks, vs, *app_args,
                                                  dev_status=status), Kd)
 
+    # copy-on-write copies of K and V blocks (all kv heads), fp16 pools
+    copies = {}
+    for n_pairs in COPY_PAIRS:
+        rng_c = np.random.default_rng(n_pairs)
+        perm = rng_c.permutation(w.num_blocks)
+        pairs = dev(np.stack([perm[:n_pairs], perm[n_pairs:2 * n_pairs]], 1).astype(np.int32))
+        fn_c = lambda: pkv.pkv_copy_blocks([kf, vf], pairs, status)
+        for _ in range(args.warmup):
+            fn_c()
+        ms_c = timed(fn_c, Kd)
+        moved = 2 * n_pairs * 2 * hkv * 16 * d * 2  # K and V, read + written
+        copies[str(n_pairs)] = {"p50_us": 1e3 * statistics.median(ms_c),
+                                "GB/s": moved / (statistics.mean(ms_c) * 1e-3) / 1e9,
+                                "frac_of_peak": moved / (statistics.mean(ms_c) * 1e-3) / 1e9
+                                / _peaks()[0],
+                                "bytes": moved}
+    bm_rate = {"native_blocks_per_s": block_manager_rate()}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        bm_rate["oracle_model_blocks_per_s"] = block_manager_rate(model=True)
+
     # eviction scoring + choice of 15 % of the blocks, at the pages' pool sizes
     evict = {}
     for nb_e in EVICT_SIZES:
@@ -554,6 +602,8 @@ def main():
                                              "tiles": 2 * ntiles,
                                              "bytes": append_bytes(ntiles, d, True)},
             "evict_select_15pct": evict,
+            "cow_copy_blocks_fp16": copies,
+            "block_manager_host": bm_rate,
         },
         "e2e": {"value": step_b * Ke / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},

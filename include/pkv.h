@@ -62,7 +62,9 @@ typedef enum pkv_status {
     PKV_ERR_UNSUPPORTED = 2, /* block_size != 16, head_dim not 64/128, size limits */
     PKV_ERR_MISALIGNED = 3,  /* a pointer misses its required alignment */
     PKV_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
-    PKV_ERR_CUDA = 5         /* a CUDA runtime call or launch failed */
+    PKV_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+    PKV_ERR_EXHAUSTED = 6    /* block manager: not enough free blocks (or host
+                                memory); nothing was changed */
 } pkv_status;
 
 /* Bits of *dev_status. */
@@ -282,6 +284,82 @@ PKV_API pkv_status pkv_evict_select(const int32_t *refcnt, const int64_t *last_u
                                     int num_blocks, int64_t current_tick, float alpha,
                                     float beta, int k, float *scores, int32_t *evict_ids,
                                     int32_t *num_evicted, void *stream);
+
+/*
+ * Block manager -- host-side bookkeeping of the physical KV blocks
+ * ([PAR] CORE CAPABILITIES 1: fixed 16-token blocks, free-list allocator,
+ * reference counting, prefix sharing, copy-on-write, fragmentation metrics;
+ * [GLO] the prefix-sharing block allocator and section 4.1.1: page-level
+ * reference counts; a shared page that diverges gets a fresh page and a
+ * copy).  Host memory only; the handle is opaque and every call locks it, so
+ * one manager may be used from several threads.  A failing call changes
+ * nothing.
+ *
+ *  - Blocks are numbered 0 .. num_blocks-1.  The free list is a stack: a
+ *    fresh manager hands out 0, 1, 2, ...; a freed block is handed out next.
+ *  - pkv_bm_allocate: one block per entry of hashes[0..n) (hashes NULL: all
+ *    0).  A nonzero hash already registered shares that block (its count + 1);
+ *    any other entry takes a free block with count 1, fill 0, and registers a
+ *    nonzero hash.  PKV_ERR_EXHAUSTED if the free list cannot serve every
+ *    entry that needs a fresh block.  Ids go to out_ids[0..n).
+ *  - pkv_bm_free: one reference dropped per entry; a block reaching count 0
+ *    loses its hash and fill and returns to the free list.
+ *    PKV_ERR_INVALID_ARG if an id is not in use or listed more often than
+ *    its count.
+ *  - pkv_bm_fork: one reference added per entry (another sequence or beam
+ *    now points at the block).
+ *  - pkv_bm_cow: for each id in order, the block to write into: the block
+ *    itself if its count is 1 (it loses any hash registration, its contents
+ *    are about to change), else a fresh block that takes one reference from
+ *    the shared one, with its fill; out_ids[i] gets it, and each
+ *    (source, fresh) pair is appended to copy_pairs (int32 [n][2], may be
+ *    NULL) for pkv_copy_blocks; *num_copies gets their number.
+ *    PKV_ERR_EXHAUSTED if not enough free blocks.
+ *  - pkv_bm_set_fill: tokens held by each block (0 .. block_size).
+ *  - pkv_bm_stats: free, used (count > 0), shared (count > 1) and logical
+ *    (sum of counts) blocks, tokens in used blocks, internal fragmentation
+ *    1 - tokens / (used * block_size), sharing saving 1 - used / logical.
+ *  - pkv_bm_refcounts: every block's count (host int32 [num_blocks]), the
+ *    refcnt input of pkv_evict_select.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+typedef struct pkv_bm_stats_t {
+    int64_t free_blocks, used_blocks, shared_blocks, logical_blocks, tokens;
+    double internal_fragmentation, sharing_saving;
+} pkv_bm_stats_t;
+
+PKV_API pkv_status pkv_bm_create(int num_blocks, int block_size, pkv_block_manager **out);
+PKV_API void pkv_bm_destroy(pkv_block_manager *bm);
+PKV_API pkv_status pkv_bm_allocate(pkv_block_manager *bm, const uint64_t *hashes, int n,
+                                   int32_t *out_ids);
+PKV_API pkv_status pkv_bm_free(pkv_block_manager *bm, const int32_t *ids, int n);
+PKV_API pkv_status pkv_bm_fork(pkv_block_manager *bm, const int32_t *ids, int n);
+PKV_API pkv_status pkv_bm_cow(pkv_block_manager *bm, const int32_t *ids, int n,
+                              int32_t *out_ids, int32_t *copy_pairs, int *num_copies);
+PKV_API pkv_status pkv_bm_set_fill(pkv_block_manager *bm, const int32_t *ids,
+                                   const int32_t *tokens, int n);
+PKV_API pkv_status pkv_bm_stats(pkv_block_manager *bm, pkv_bm_stats_t *out);
+PKV_API pkv_status pkv_bm_refcounts(pkv_block_manager *bm, int32_t *out, int n);
+
+/*
+ * pkv_copy_blocks -- the copies that copy-on-write asks for ([GLO] section
+ * 4.1.1), batched: for every pair (pairs[i][0] = source, pairs[i][1] =
+ * destination block), the block's bytes in every pool are copied.
+ *
+ *   pools        host array of num_pools (<= 8) device pointers, each a pool
+ *                laid out [num_blocks][...] with block_bytes[p] bytes per
+ *                block (K and V pools: num_kv_heads * 16 * head_dim * element
+ *                size; INT8 scales: num_kv_heads * 4); 4-byte aligned, block
+ *                sizes multiples of 4 (16-byte units where both allow)
+ *   pairs        device int32 [num_pairs][2]
+ * A pair naming a block outside [0, num_blocks) sets PKV_DEV_BAD_BLOCK and is
+ * skipped; a pair with source == destination is a no-op.  Destinations must
+ * be distinct and must not be sources of the same call.
+ */
+PKV_API pkv_status pkv_copy_blocks(void *const *pools, const int64_t *block_bytes,
+                                   int num_pools, int num_blocks, const int32_t *pairs,
+                                   int num_pairs, int32_t *dev_status, void *stream);
 
 /*
  * Bytes of workspace a decode call with these sizes needs (either variant).

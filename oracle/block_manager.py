@@ -146,6 +146,28 @@ class BlockManagerModel:
         self.hash_of[n] = NO_HASH
         return n, True
 
+    def cow_batch(self, ids):
+        """``cow`` of each id in order, all-or-nothing: returns (blocks to
+        write, [(source, copy)] pairs) or None (nothing changed)."""
+        ids = [int(b) for b in ids]
+        if not self._check_ids(ids):
+            return None
+        left, copies = {}, 0
+        for b in ids:
+            c = left.setdefault(b, self.refcnt[b])
+            if c > 1:
+                left[b] = c - 1
+                copies += 1
+        if copies > len(self.free_list):
+            return None
+        out, pairs = [], []
+        for b in ids:
+            nb, copied = self.cow(b)
+            out.append(nb)
+            if copied:
+                pairs.append((b, nb))
+        return out, pairs
+
     def set_fill(self, ids, tokens) -> bool:
         ids = [int(b) for b in ids]
         tokens = [int(t) for t in tokens]

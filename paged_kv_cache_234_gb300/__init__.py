@@ -14,6 +14,9 @@ The functions carry the C names and take torch tensors:
 * ``pkv_append_fp16``         write one new token per sequence into fp16 pools
 * ``pkv_append_int8``         the same, re-quantizing every tile it writes
 * ``pkv_evict_select``        eviction scores of every block + the k to evict
+* ``BlockManager``            host block manager (``pkv_bm_*``: free list,
+                              reference counts, prefix sharing, copy-on-write)
+* ``pkv_copy_blocks``         the batched block copies copy-on-write asks for
 * ``pkv_decode_workspace_size``, ``pkv_set_decode_workers``,
   ``pkv_status_string``
 """
@@ -33,6 +36,7 @@ PKV_ERR_UNSUPPORTED = 2
 PKV_ERR_MISALIGNED = 3
 PKV_ERR_WORKSPACE = 4
 PKV_ERR_CUDA = 5
+PKV_ERR_EXHAUSTED = 6
 
 PKV_DEV_BAD_BLOCK = 1
 PKV_DEV_BAD_CTX = 2
@@ -40,8 +44,10 @@ PKV_DEV_TIMEOUT = 4
 
 EXPORTED = ("pkv_quantize_blocks", "pkv_paged_decode_fp16", "pkv_paged_decode_int8",
             "pkv_paged_decode_int8_static_workspace", "pkv_append_fp16", "pkv_append_int8",
-            "pkv_evict_select", "pkv_decode_workspace_size", "pkv_set_decode_workers",
-            "pkv_status_string")
+            "pkv_evict_select", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_allocate",
+            "pkv_bm_free", "pkv_bm_fork", "pkv_bm_cow", "pkv_bm_set_fill", "pkv_bm_stats",
+            "pkv_bm_refcounts", "pkv_copy_blocks", "pkv_decode_workspace_size",
+            "pkv_set_decode_workers", "pkv_status_string")
 
 # weights of the least-reference-count + age eviction score
 EVICT_ALPHA = 0.7
@@ -52,6 +58,13 @@ PKV_STATIC_WORKSPACE_BYTES = 32 << 20
 
 _lock = threading.Lock()
 _lib = None
+
+
+class BmStats(ctypes.Structure):
+    _fields_ = [("free_blocks", ctypes.c_int64), ("used_blocks", ctypes.c_int64),
+                ("shared_blocks", ctypes.c_int64), ("logical_blocks", ctypes.c_int64),
+                ("tokens", ctypes.c_int64), ("internal_fragmentation", ctypes.c_double),
+                ("sharing_saving", ctypes.c_double)]
 
 
 class PkvError(RuntimeError):
@@ -88,6 +101,25 @@ def lib() -> ctypes.CDLL:
         L.pkv_append_int8.argtypes = app[:2] + [P, P, P, P] + app[2:]
         L.pkv_evict_select.restype = I
         L.pkv_evict_select.argtypes = [P, P, I, ctypes.c_int64, F, F, I, P, P, P, P]
+        L.pkv_bm_create.restype = I
+        L.pkv_bm_create.argtypes = [I, I, ctypes.POINTER(P)]
+        L.pkv_bm_destroy.restype = None
+        L.pkv_bm_destroy.argtypes = [P]
+        L.pkv_bm_allocate.restype = I
+        L.pkv_bm_allocate.argtypes = [P, P, I, P]
+        for name in ("pkv_bm_free", "pkv_bm_fork"):
+            getattr(L, name).restype = I
+            getattr(L, name).argtypes = [P, P, I]
+        L.pkv_bm_cow.restype = I
+        L.pkv_bm_cow.argtypes = [P, P, I, P, P, ctypes.POINTER(I)]
+        L.pkv_bm_set_fill.restype = I
+        L.pkv_bm_set_fill.argtypes = [P, P, P, I]
+        L.pkv_bm_stats.restype = I
+        L.pkv_bm_stats.argtypes = [P, ctypes.POINTER(BmStats)]
+        L.pkv_bm_refcounts.restype = I
+        L.pkv_bm_refcounts.argtypes = [P, P, I]
+        L.pkv_copy_blocks.restype = I
+        L.pkv_copy_blocks.argtypes = [P, P, I, I, P, I, P, P]
         L.pkv_decode_workspace_size.restype = Z
         L.pkv_decode_workspace_size.argtypes = [I, I, I, I, I]
         L.pkv_set_decode_workers.restype = I
@@ -313,3 +345,113 @@ def evict_count(num_blocks: int, percent: int = 15) -> int:
     if num_blocks < 0 or not 0 <= percent <= 100:
         raise ValueError("bad block count or percentage")
     return (int(num_blocks) * int(percent)) // 100
+
+
+def _np_i32(x):
+    import numpy as np
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32).reshape(-1))
+
+
+class BlockManager:
+    """The library's host block manager (``pkv_bm_*``).  Ids are numpy int32
+    arrays; a failing call raises PkvError and changes nothing."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        h = ctypes.c_void_p()
+        st = lib().pkv_bm_create(int(num_blocks), int(block_size), ctypes.byref(h))
+        if st != PKV_OK:
+            raise PkvError(st, "pkv_bm_create")
+        self._h = h
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _call(self, name, *args):
+        st = getattr(lib(), name)(self._h, *args)
+        if st != PKV_OK:
+            raise PkvError(st, name)
+
+    def allocate(self, hashes):
+        """hashes: an int (that many blocks, no hash) or a sequence of uint64
+        prefix hashes (0 = none).  Returns the block ids."""
+        import numpy as np
+        if isinstance(hashes, int):
+            n, hp = hashes, None
+        else:
+            hp = np.ascontiguousarray(np.asarray(hashes, dtype=np.uint64).reshape(-1))
+            n = hp.size
+        out = np.empty(n, np.int32)
+        self._call("pkv_bm_allocate", None if hp is None else hp.ctypes.data, n,
+                   out.ctypes.data)
+        return out
+
+    def free(self, ids):
+        a = _np_i32(ids)
+        self._call("pkv_bm_free", a.ctypes.data, a.size)
+
+    def fork(self, ids):
+        a = _np_i32(ids)
+        self._call("pkv_bm_fork", a.ctypes.data, a.size)
+
+    def cow(self, ids):
+        """Returns (blocks to write, (source, copy) pairs int32 [k][2])."""
+        import numpy as np
+        a = _np_i32(ids)
+        out = np.empty(a.size, np.int32)
+        pairs = np.empty((a.size, 2), np.int32)
+        k = ctypes.c_int(0)
+        self._call("pkv_bm_cow", a.ctypes.data, a.size, out.ctypes.data, pairs.ctypes.data,
+                   ctypes.byref(k))
+        return out, pairs[:k.value].copy()
+
+    def set_fill(self, ids, tokens):
+        a, t = _np_i32(ids), _np_i32(tokens)
+        if a.size != t.size:
+            raise ValueError("ids and tokens differ in length")
+        self._call("pkv_bm_set_fill", a.ctypes.data, t.ctypes.data, a.size)
+
+    def stats(self) -> dict:
+        st = BmStats()
+        self._call("pkv_bm_stats", ctypes.byref(st))
+        return {"free": st.free_blocks, "used": st.used_blocks, "shared": st.shared_blocks,
+                "logical": st.logical_blocks, "tokens": st.tokens,
+                "internal_fragmentation": st.internal_fragmentation,
+                "sharing_saving": st.sharing_saving}
+
+    def refcounts(self):
+        import numpy as np
+        out = np.empty(self.num_blocks, np.int32)
+        self._call("pkv_bm_refcounts", out.ctypes.data, self.num_blocks)
+        return out
+
+
+def pkv_copy_blocks(pools, pairs, dev_status=None, stream=None) -> None:
+    """Copy block pairs[i][0] to block pairs[i][1] in every pool (CUDA
+    tensors shaped [num_blocks, ...], contiguous); pairs: int32 [n][2] CUDA."""
+    import torch
+    _check(pairs, "pairs", torch.int32)
+    _check(dev_status, "dev_status", torch.int32)
+    nb = pools[0].shape[0]
+    ptrs = (ctypes.c_void_p * len(pools))()
+    sizes = (ctypes.c_int64 * len(pools))()
+    for i, t in enumerate(pools):
+        _check(t, f"pools[{i}]")
+        if t.shape[0] != nb:
+            raise ValueError("all pools must have the same number of blocks")
+        ptrs[i] = t.data_ptr()
+        sizes[i] = (t.numel() // nb) * t.element_size()
+    st = lib().pkv_copy_blocks(ptrs, sizes, len(pools), nb, _ptr(pairs),
+                               0 if pairs is None else pairs.shape[0], _ptr(dev_status),
+                               _stream(stream))
+    if st != PKV_OK:
+        raise PkvError(st, "pkv_copy_blocks")

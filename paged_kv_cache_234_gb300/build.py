@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libpkv.so")
 INCLUDE = os.path.join(os.path.dirname(PKG_DIR), "include")
-SOURCES = ("pkv_host.cu", "pkv_quantize.cu", "pkv_decode.cu", "pkv_append.cu", "pkv_evict.cu")
+SOURCES = ("pkv_host.cu", "pkv_quantize.cu", "pkv_decode.cu", "pkv_append.cu", "pkv_evict.cu",
+           "pkv_copy.cu", "pkv_block_manager.cpp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

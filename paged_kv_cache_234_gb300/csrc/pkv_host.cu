@@ -80,6 +80,7 @@ extern "C" const char *pkv_status_string(pkv_status status)
     case PKV_ERR_MISALIGNED: return "misaligned pointer";
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
     case PKV_ERR_CUDA: return "CUDA runtime or launch failure";
+    case PKV_ERR_EXHAUSTED: return "no free block (or host memory) for the request";
     }
     return "unknown status";
 }

@@ -162,6 +162,23 @@ def test_evict_host_validation(L):
     assert e(scores=FAKE + 2) == pkv.PKV_ERR_MISALIGNED
 
 
+def test_copy_blocks_host_validation(L):
+    P2 = ctypes.c_void_p * 2
+    S2 = ctypes.c_int64 * 2
+    def c(pools=(FAKE, FAKE), sizes=(4096, 32), n=2, nb=16, pairs=FAKE, npairs=3):
+        return L.pkv_copy_blocks(P2(*pools), S2(*sizes), n, nb, pairs, npairs, None, None)
+    assert c(n=0) == pkv.PKV_ERR_INVALID_ARG
+    assert c(nb=0) == pkv.PKV_ERR_INVALID_ARG
+    assert c(npairs=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert c(pairs=None) == pkv.PKV_ERR_INVALID_ARG
+    assert c(pools=(FAKE, None)) == pkv.PKV_ERR_INVALID_ARG
+    assert c(sizes=(4096, 0)) == pkv.PKV_ERR_INVALID_ARG
+    assert c(sizes=(4096, 30)) == pkv.PKV_ERR_MISALIGNED
+    assert c(pools=(FAKE + 2, FAKE)) == pkv.PKV_ERR_MISALIGNED
+    assert c(n=9) == pkv.PKV_ERR_UNSUPPORTED
+    assert c(npairs=0) == pkv.PKV_OK  # nothing launched
+
+
 # The PagedKV-Fusion README's end-to-end demos evict 15 % of the scored
 # blocks: 173 of 1155 (CPU reference) and 85 of 568 (CUDA run).
 def test_evict_count_matches_the_pages_examples():
