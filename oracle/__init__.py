@@ -20,6 +20,9 @@ Every function cites the passage it follows:
   Overview component B; Architecture "per-block,head symmetric INT8"), with
   the absmax/127 scale and round-half-to-even reading.
 * ``kv_pool_mib`` -- the storage arithmetic of the Memory footprint table.
+* ``quantize_fp8`` / ``decode_fp8`` / ``e4m3_*`` -- per-block scaled FP8
+  (OCP E4M3) keys and values ("PagedAttention & KV-Cache Memory Management",
+  section 5.1), scale = amax / 448, decoded exactly.
 * ``append_fp16`` / ``append_int8`` -- the write of one new token per
   sequence at slot table[s][t / B] * B + t % B ("PagedAttention & KV-Cache
   Memory Management", section 2.1 and the prefill step of its kernel
@@ -94,6 +97,12 @@ def _load():
         lib.pkv_oracle_quantize.argtypes = [
             P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
             ctypes.c_int, ctypes.c_int]
+        lib.pkv_oracle_quantize_fp8.restype = ctypes.c_int64
+        lib.pkv_oracle_quantize_fp8.argtypes = lib.pkv_oracle_quantize.argtypes
+        lib.pkv_oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.pkv_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.pkv_oracle_e4m3_from_float.restype = ctypes.c_uint8
+        lib.pkv_oracle_e4m3_from_float.argtypes = [ctypes.c_float]
         lib.pkv_oracle_append.restype = ctypes.c_int64
         lib.pkv_oracle_append.argtypes = [
             P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -138,7 +147,8 @@ def _decode(kind, query, kpool, vpool, kscale, vscale, block_tables,
         kp, vp = _c(kpool, np.float16), _c(vpool, np.float16)
         ks = vs = None
     else:
-        kp, vp = _c(kpool, np.int8), _c(vpool, np.int8)
+        cdt = np.int8 if kind == 1 else np.uint8
+        kp, vp = _c(kpool, cdt), _c(vpool, cdt)
         ks, vs = _c(kscale, np.float32), _c(vscale, np.float32)
     nb = kp.shape[0]
     assert kp.shape == (nb, num_kv_heads, block_size, d) and vp.shape == kp.shape
@@ -313,3 +323,48 @@ def evict_select(refcnt, last_used, current_tick, k, alpha=EVICT_ALPHA, beta=EVI
     if n < 0:
         raise ValueError("oracle rejected the eviction arguments")
     return ids[:n].copy(), scores
+
+
+def decode_fp8(query, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, *,
+               num_kv_heads, softmax_scale, block_size=16, max_context_len=None,
+               num_threads=0, return_flags=False):
+    """fp64 paged decode attention over FP8 (E4M3 bytes) pools,
+    value = e4m3(code) * scale ("PagedAttention & KV-Cache Memory
+    Management", section 5.1)."""
+    return _decode(2, query, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens,
+                   num_kv_heads, block_size, max_context_len, softmax_scale, num_threads,
+                   return_flags)
+
+
+def e4m3_to_double(code: int) -> float:
+    return _load().pkv_oracle_e4m3_to_double(int(code) & 0xFF)
+
+
+def e4m3_from_float(y: float) -> int:
+    """Nearest finite E4M3 code of a non-NaN fp32 value (ties to even,
+    saturating at +-448)."""
+    return int(_load().pkv_oracle_e4m3_from_float(float(y)))
+
+
+def quantize_fp8(pool, block_ids=None, code_pool=None, scales=None, inplace=False):
+    """Per-(block, kv-head) FP8 E4M3 quantization of an fp16 pool: scale =
+    fp32 amax / 448, code = E4M3 of the fp32 quotient x / scale (a NaN
+    quotient gives 0).  Arguments and results as ``quantize`` with uint8
+    codes."""
+    lib = _load()
+    x = _c(pool, np.float16)
+    nb, hkv, bs, d = x.shape
+    if inplace:
+        codes, sc = code_pool, scales
+        assert codes.flags.c_contiguous and codes.dtype == np.uint8 and codes.shape == x.shape
+        assert sc.flags.c_contiguous and sc.dtype == np.float32 and sc.shape == (nb, hkv)
+    else:
+        codes = np.zeros(x.shape, np.uint8) if code_pool is None else _c(code_pool, np.uint8).copy()
+        sc = np.zeros((nb, hkv), np.float32) if scales is None else _c(scales, np.float32).copy()
+    ids = None if block_ids is None else _c(block_ids, np.int32).reshape(-1)
+    nids = 0 if ids is None else ids.size
+    bad = lib.pkv_oracle_quantize_fp8(_ptr(codes), _ptr(sc), _ptr(x), _ptr(ids), nids,
+                                      nb, hkv, bs, d)
+    if bad < 0:
+        raise ValueError("oracle rejected the quantize arguments")
+    return codes, sc

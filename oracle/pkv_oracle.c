@@ -36,6 +36,16 @@
  *    design notes).  Computed in fp32 so that codes and scales can be
  *    compared bit for bit.
  *
+ *  - FP8 KV ("PagedAttention & KV-Cache Memory Management", section 5.1:
+ *    per-block scaled FP8 keys and values, scale_k / scale_v per block):
+ *    pkv_oracle_e4m3_to_double decodes an OCP E4M3 byte (sign, 4 exponent
+ *    bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN,
+ *    largest finite 448); pkv_oracle_e4m3_from_float picks the nearest finite
+ *    E4M3 value of an fp32 number by searching all of them (ties to the code
+ *    with an even last bit), saturating at +-448; pkv_oracle_quantize_fp8
+ *    quantizes a tile with scale = amax / 448 exactly as the INT8 quantizer
+ *    does with 127 (a NaN quotient gives code 0).
+ *
  *  - pkv_oracle_append: the write that precedes a decode step.  The new
  *    token of sequence s sits at position t = positions[s]; its K and V rows
  *    (one per kv head) go to slot t % B of physical block table[s][t / B]
@@ -96,6 +106,34 @@ double pkv_oracle_half_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/* Exact value of an E4M3 byte: (8 + m) * 2^(e - 10) for e > 0, m * 2^-9 for
+   e == 0; NaN for exponent and mantissa all ones. */
+double pkv_oracle_e4m3_to_double(uint8_t c)
+{
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return sign ? -v : v;
+}
+
+/* Nearest finite E4M3 code of a non-NaN fp32 value; ties go to the code with
+   an even mantissa bit 0; magnitudes beyond 448 give +-448. */
+uint8_t pkv_oracle_e4m3_from_float(float y)
+{
+    const int sign = signbit(y) ? 1 : 0;
+    const double a = fabs((double)y);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) { /* every finite non-negative code */
+        const double err = fabs(pkv_oracle_e4m3_to_double((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)((sign << 7) | best);
+}
+
 /* One element of K or V for token slot `slot` of physical block `blk`. */
 static double kv_element(int kv_kind, const void *pool, const float *scales,
                          int64_t blk, int kvh, int slot, int i,
@@ -105,6 +143,9 @@ static double kv_element(int kv_kind, const void *pool, const float *scales,
     const int64_t idx = (tile * block_size + slot) * head_dim + i;
     if (kv_kind == 0) {
         return pkv_oracle_half_to_double(((const uint16_t *)pool)[idx]);
+    }
+    if (kv_kind == 2) {
+        return pkv_oracle_e4m3_to_double(((const uint8_t *)pool)[idx]) * (double)scales[tile];
     }
     return (double)((const int8_t *)pool)[idx] * (double)scales[tile];
 }
@@ -126,7 +167,7 @@ int pkv_oracle_decode(double *out, const uint16_t *query, int kv_kind,
 {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
         num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
-        max_blocks_per_seq < 0 || (kv_kind != 0 && kv_kind != 1)) {
+        max_blocks_per_seq < 0 || kv_kind < 0 || kv_kind > 2) {
         return -1;
     }
     const int group = num_heads / num_kv_heads;
@@ -227,6 +268,46 @@ static void quantize_tile(int8_t *codes, float *scale_out, const uint16_t *x, in
         codes[e] = (int8_t)c;
     }
     *scale_out = scale;
+}
+
+/* FP8 version of quantize_tile: scale = amax / 448, code = E4M3 of x / scale. */
+static void quantize_tile_fp8(uint8_t *codes, float *scale_out, const uint16_t *x, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t e = 0; e < n; ++e) {
+        const float a = fabsf((float)pkv_oracle_half_to_double(x[e]));
+        if (a > amax) amax = a; /* NaN never compares greater: ignored */
+    }
+    const float scale = amax / 448.0f;
+    for (int64_t e = 0; e < n; ++e) {
+        const float v = (float)pkv_oracle_half_to_double(x[e]);
+        const float y = v / scale; /* 0/0 and inf/inf give NaN -> code 0 */
+        codes[e] = isnan(y) ? 0 : pkv_oracle_e4m3_from_float(y);
+    }
+    *scale_out = scale;
+}
+
+int64_t pkv_oracle_quantize_fp8(uint8_t *code_pool, float *scales, const uint16_t *pool,
+                                const int32_t *block_ids, int64_t num_ids, int64_t num_blocks,
+                                int num_kv_heads, int block_size, int head_dim)
+{
+    if (num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 || head_dim <= 0) return -1;
+    const int64_t tile_elems = (int64_t)block_size * head_dim;
+    const int64_t count = block_ids ? num_ids : num_blocks;
+    int64_t bad = 0;
+    for (int64_t j = 0; j < count; ++j) {
+        const int64_t blk = block_ids ? block_ids[j] : j;
+        if (blk < 0 || blk >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        for (int kvh = 0; kvh < num_kv_heads; ++kvh) {
+            const int64_t tile = blk * num_kv_heads + kvh;
+            quantize_tile_fp8(code_pool + tile * tile_elems, scales + tile,
+                              pool + tile * tile_elems, tile_elems);
+        }
+    }
+    return bad;
 }
 
 /*
