@@ -10,7 +10,7 @@ Workload: 64 seqs x ctx 2048, 32 q / 8 kv heads, head_dim 128, block 16, a
 
 Metric: KV GB/s = algorithmic bytes per step / step time (the bytes of K, V
 and scales a step must read plus what the quantizer reads and writes), also
-sequence-steps/s and p50 us/step.  The fp16-KV decode of the same batch, the
+sequence-steps/s and p50 us/step.  The fp16-KV and FP8-KV decodes of the same batch, the
 token append that precedes a decode step (fp16, and INT8 with the fused tail
 re-quantize), eviction scoring + choice of 15 % of the blocks at pools of
 1024, 16384 and 65536 blocks, the copy-on-write block copies (64 and 4096
@@ -285,15 +285,22 @@ def run_profile(args):
         vs = torch.zeros_like(ks)
         tails = dev(w.tail_block_ids())
         call = lambda: pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, tails)
-    elif args.profile == "int8":
+    elif args.profile in ("int8", "fp8"):
         kc = torch.zeros(w.k_pool.shape, dtype=torch.int8, device="cuda")
         vc = torch.zeros_like(kc)
         ks = torch.zeros(w.k_pool.shape[:2], dtype=torch.float32, device="cuda")
         vs = torch.zeros_like(ks)
-        pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, dev(w.used_block_ids))
+        if args.profile == "fp8":
+            kc = kc.view(torch.uint8)
+            vc = vc.view(torch.uint8)
+            pkv.pkv_quantize_blocks_fp8(kf, vf, kc, vc, ks, vs, dev(w.used_block_ids))
+            dec = pkv.pkv_paged_decode_fp8
+        else:
+            pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, dev(w.used_block_ids))
+            dec = pkv.pkv_paged_decode_int8
         del kf, vf
-        call = lambda: pkv.pkv_paged_decode_int8(out, q, kc, vc, ks, vs, bt, cl,
-                                                 w.max_context_len, w.softmax_scale, ws_t)
+        call = lambda: dec(out, q, kc, vc, ks, vs, bt, cl, w.max_context_len, w.softmax_scale,
+                           ws_t)
     else:
         call = lambda: pkv.pkv_paged_decode_fp16(out, q, kf, vf, bt, cl, w.max_context_len,
                                                  w.softmax_scale, ws_t)
@@ -358,7 +365,7 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["int8", "fp16", "quantize", "append", "evict"],
+    ap.add_argument("--profile", choices=["int8", "fp8", "fp16", "quantize", "append", "evict"],
                     help="profiling run: the same batch over a 16384-block pool (eviction: "
                          "a 65536-block pool), only warm-up + timed calls of one kernel, "
                          "no report line")
@@ -419,6 +426,11 @@ def main():
 
     # the cache contents: every used block quantized once (not timed)
     pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, used, status)
+    kc8 = torch.zeros(w.k_pool.shape, dtype=torch.uint8, device="cuda")
+    vc8 = torch.zeros_like(kc8)
+    ks8 = torch.zeros_like(ks)
+    vs8 = torch.zeros_like(ks)
+    pkv.pkv_quantize_blocks_fp8(kf, vf, kc8, vc8, ks8, vs8, used, status)
     torch.cuda.synchronize()
 
     def step_int8():
@@ -428,6 +440,10 @@ def main():
         pkv.pkv_paged_decode_int8(out, q, kc, vc, ks, vs, bt, cl, mcl, w.softmax_scale, ws_t,
                                   status)
 
+    def decode_fp8():
+        pkv.pkv_paged_decode_fp8(out, q, kc8, vc8, ks8, vs8, bt, cl, mcl, w.softmax_scale, ws_t,
+                                 status)
+
     def decode_fp16():
         pkv.pkv_paged_decode_fp16(out, q, kf, vf, bt, cl, mcl, w.softmax_scale, ws_t, status)
 
@@ -435,6 +451,7 @@ def main():
         step_int8()
         decode_int8()
         decode_fp16()
+        decode_fp8()
     torch.cuda.synchronize()
 
     K = args.steps
@@ -475,6 +492,7 @@ def main():
     Kd = min(K, 500)
     dec_ms = timed(decode_int8, Kd)
     f16_ms = timed(decode_fp16, Kd)
+    f8_ms = timed(decode_fp8, Kd)
     q_ms = timed(step_int8, Kd)
 
     # the write before a decode step: every sequence's newest token appended
@@ -593,6 +611,10 @@ def main():
                             "bytes": f16_b},
             "decode_int8": {"p50_us": 1e3 * statistics.median(dec_ms), "GB/s": achieved,
                             "bytes": dec_b},
+            "decode_fp8": {"p50_us": 1e3 * statistics.median(f8_ms),
+                           "GB/s": dec_b / (statistics.mean(f8_ms) * 1e-3) / 1e9,
+                           "frac_of_peak": dec_b / (statistics.mean(f8_ms) * 1e-3) / 1e9 / peak,
+                           "bytes": dec_b},
             "quantize_tail_blocks": {"p50_us": 1e3 * statistics.median(q_ms),
                                      "tiles": 2 * ntiles,
                                      "bytes": quantize_bytes(ntiles, d)},

@@ -17,7 +17,8 @@
  *  [GLO]  "PagedAttention & KV-Cache Memory Management": section 2.1 (block
  *         table: block = table[t / B], slot = t % B; "Kernel Mechanics":
  *         token writes), 3.3.2 (appending tokens), 4.3.1 (least-reference-
- *         count + age eviction score).
+ *         count + age eviction score), 4.1.1 (copy-on-write), 5.1 (per-block
+ *         scaled FP8 KV).
  *
  * Layouts (all row-major, all pointers are DEVICE pointers owned by the
  * caller; the library never allocates, frees or synchronises):
@@ -165,6 +166,42 @@ PKV_API pkv_status pkv_paged_decode_int8(float *out, const void *query,
                                  int block_size, float softmax_scale,
                                  void *workspace, size_t workspace_bytes,
                                  int32_t *dev_status, void *stream);
+
+/*
+ * pkv_quantize_blocks_fp8 -- pkv_quantize_blocks with FP8 codes: OCP E4M3
+ * bytes (sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, largest finite 448) with one fp32 scale per (block, kv head)
+ * for K and one for V ([GLO] section 5.1: per-block scaled FP8 keys and
+ * values).  For every value x of the tile:
+ *   scale = amax / 448 (IEEE fp32 division; amax = max |x|, NaN ignored)
+ *   code  = the E4M3 value nearest to the fp32 quotient x / scale (ties to
+ *           even), saturated to +-448; a NaN quotient gives code 0
+ * Arguments as pkv_quantize_blocks, with uint8 code pools.  Bit-identical to
+ * the CPU oracle of this repository.
+ */
+PKV_API pkv_status pkv_quantize_blocks_fp8(const void *k_fp16, const void *v_fp16,
+                                           uint8_t *k_codes, uint8_t *v_codes,
+                                           float *k_scales, float *v_scales,
+                                           const int32_t *block_ids, int num_ids,
+                                           int num_blocks, int num_kv_heads, int head_dim,
+                                           int block_size, int32_t *dev_status, void *stream);
+
+/*
+ * pkv_paged_decode_fp8 -- the decode step over FP8 (E4M3) codes with per-
+ * (block, kv head) scales, as produced by pkv_quantize_blocks_fp8:
+ * K_t = e4m3(k_codes[...]) * k_scales[blk][kvh], V_t likewise.  Arguments as
+ * pkv_paged_decode_int8 with uint8 code pools.
+ */
+PKV_API pkv_status pkv_paged_decode_fp8(float *out, const void *query,
+                                        const uint8_t *k_codes, const uint8_t *v_codes,
+                                        const float *k_scales, const float *v_scales,
+                                        int num_blocks, const int32_t *block_tables,
+                                        int max_blocks_per_seq, const int32_t *context_lens,
+                                        int max_context_len, int num_seqs, int num_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        float softmax_scale, void *workspace,
+                                        size_t workspace_bytes, int32_t *dev_status,
+                                        void *stream);
 
 /*
  * pkv_paged_decode_int8_static_workspace -- pkv_paged_decode_int8 for

@@ -40,9 +40,9 @@
  *    per-block scaled FP8 keys and values, scale_k / scale_v per block):
  *    pkv_oracle_e4m3_to_double decodes an OCP E4M3 byte (sign, 4 exponent
  *    bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN,
- *    largest finite 448); pkv_oracle_e4m3_from_float picks the nearest finite
- *    E4M3 value of an fp32 number by searching all of them (ties to the code
- *    with an even last bit), saturating at +-448; pkv_oracle_quantize_fp8
+ *    largest finite 448); pkv_oracle_e4m3_from_float rounds an fp32 number
+ *    to the nearest finite E4M3 value (ties to the code with an even last
+ *    bit), saturating at +-448; pkv_oracle_quantize_fp8
  *    quantizes a tile with scale = amax / 448 exactly as the INT8 quantizer
  *    does with 127 (a NaN quotient gives code 0).
  *
@@ -116,22 +116,34 @@ double pkv_oracle_e4m3_to_double(uint8_t c)
     return sign ? -v : v;
 }
 
-/* Nearest finite E4M3 code of a non-NaN fp32 value; ties go to the code with
-   an even mantissa bit 0; magnitudes beyond 448 give +-448. */
+/* Nearest finite E4M3 code of a non-NaN fp32 value; ties go to the code
+   with an even last bit; magnitudes beyond 448 give +-448.  The grid: below
+   2^-6 the step is 2^-9 (subnormals, code = multiple of the step); in the
+   binade [2^E, 2^(E+1)) the step is 2^(E-3), code = (E + 7) << 3 | (q - 8)
+   with q = a / 2^(E-3) in [8, 16).  q is rounded to nearest-even in double
+   (a and the power-of-two scaling are exact). */
 uint8_t pkv_oracle_e4m3_from_float(float y)
 {
     const int sign = signbit(y) ? 1 : 0;
     const double a = fabs((double)y);
-    int best = 0;
-    double best_err = INFINITY;
-    for (int c = 0; c <= 0x7E; ++c) { /* every finite non-negative code */
-        const double err = fabs(pkv_oracle_e4m3_to_double((uint8_t)c) - a);
-        if (err < best_err || (err == best_err && (c & 1) == 0)) {
-            best = c;
-            best_err = err;
+    int code;
+    if (a > 448.0) {
+        code = 0x7E;
+    } else if (a < ldexp(1.0, -6)) {
+        code = (int)nearbyint(ldexp(a, 9)); /* 0 .. 8; 8 is 2^-6, the first normal */
+    } else {
+        int k;
+        (void)frexp(a, &k);                 /* a = f * 2^k, f in [0.5, 1) */
+        int e = k - 1;                      /* a in [2^e, 2^(e+1)) */
+        int q = (int)nearbyint(ldexp(a, 3 - e));
+        if (q == 16) {                      /* rounded up into the next binade */
+            q = 8;
+            ++e;
         }
+        code = ((e + 7) << 3) | (q - 8);
+        if (code > 0x7E) code = 0x7E;       /* 464 and up saturate */
     }
-    return (uint8_t)((sign << 7) | best);
+    return (uint8_t)((sign << 7) | code);
 }
 
 /* One element of K or V for token slot `slot` of physical block `blk`. */

@@ -11,6 +11,8 @@ The functions carry the C names and take torch tensors:
 * ``pkv_quantize_blocks``     fp16 K/V tiles -> INT8 codes + fp32 scales
 * ``pkv_paged_decode_fp16``   decode-step attention over fp16 K/V pools
 * ``pkv_paged_decode_int8``   decode-step attention over INT8 K/V pools
+* ``pkv_quantize_blocks_fp8`` fp16 K/V tiles -> FP8 (E4M3) codes + fp32 scales
+* ``pkv_paged_decode_fp8``    decode-step attention over FP8 K/V pools
 * ``pkv_append_fp16``         write one new token per sequence into fp16 pools
 * ``pkv_append_int8``         the same, re-quantizing every tile it writes
 * ``pkv_evict_select``        eviction scores of every block + the k to evict
@@ -43,6 +45,7 @@ PKV_DEV_BAD_CTX = 2
 PKV_DEV_TIMEOUT = 4
 
 EXPORTED = ("pkv_quantize_blocks", "pkv_paged_decode_fp16", "pkv_paged_decode_int8",
+            "pkv_quantize_blocks_fp8", "pkv_paged_decode_fp8",
             "pkv_paged_decode_int8_static_workspace", "pkv_append_fp16", "pkv_append_int8",
             "pkv_evict_select", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_allocate",
             "pkv_bm_free", "pkv_bm_fork", "pkv_bm_cow", "pkv_bm_set_fill", "pkv_bm_stats",
@@ -92,6 +95,10 @@ def lib() -> ctypes.CDLL:
         L.pkv_paged_decode_fp16.argtypes = dec
         L.pkv_paged_decode_int8.restype = I
         L.pkv_paged_decode_int8.argtypes = dec[:4] + [P, P] + dec[4:]
+        L.pkv_paged_decode_fp8.restype = I
+        L.pkv_paged_decode_fp8.argtypes = dec[:4] + [P, P] + dec[4:]
+        L.pkv_quantize_blocks_fp8.restype = I
+        L.pkv_quantize_blocks_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P]
         L.pkv_paged_decode_int8_static_workspace.restype = I
         L.pkv_paged_decode_int8_static_workspace.argtypes = dec[:4] + [P, P] + dec[4:15] + dec[17:]
         app = [P, P, I, P, P, P, I, P, I, I, I, I, P, P]
@@ -170,23 +177,37 @@ def pkv_set_decode_workers(max_workers: int) -> None:
 def pkv_quantize_blocks(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
                         block_ids=None, dev_status=None, stream=None) -> None:
     """Quantize the (block, kv head) tiles of fp16 pools [NB][Hkv][16][d]."""
+    _quantize("pkv_quantize_blocks", k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
+              block_ids, dev_status, stream)
+
+
+def pkv_quantize_blocks_fp8(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
+                            block_ids=None, dev_status=None, stream=None) -> None:
+    """FP8 (E4M3, uint8 code pools) quantization of the tiles of fp16 pools."""
+    _quantize("pkv_quantize_blocks_fp8", k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
+              block_ids, dev_status, stream)
+
+
+def _quantize(fn_name, k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, block_ids,
+              dev_status, stream):
     import torch
+    code_t = torch.uint8 if fn_name.endswith("fp8") else torch.int8
     _check(k_fp16, "k_fp16", torch.float16)
     _check(v_fp16, "v_fp16", torch.float16)
-    _check(k_codes, "k_codes", torch.int8)
-    _check(v_codes, "v_codes", torch.int8)
+    _check(k_codes, "k_codes", code_t)
+    _check(v_codes, "v_codes", code_t)
     _check(k_scales, "k_scales", torch.float32)
     _check(v_scales, "v_scales", torch.float32)
     _check(block_ids, "block_ids", torch.int32)
     _check(dev_status, "dev_status", torch.int32)
     nb, hkv, bs, d = k_fp16.shape
     nids = 0 if block_ids is None else block_ids.numel()
-    st = lib().pkv_quantize_blocks(
+    st = getattr(lib(), fn_name)(
         _ptr(k_fp16), _ptr(v_fp16), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
         _ptr(v_scales), _ptr(block_ids), nids, nb, hkv, d, bs, _ptr(dev_status),
         _stream(stream))
     if st != PKV_OK:
-        raise PkvError(st, "pkv_quantize_blocks")
+        raise PkvError(st, fn_name)
 
 
 def _decode(fn_name, out, query, kp, vp, ks, vs, block_tables, context_lens,
@@ -234,6 +255,20 @@ def pkv_paged_decode_int8(out, query, k_codes, v_codes, k_scales, v_scales, bloc
     _check(k_scales, "k_scales", torch.float32)
     _check(v_scales, "v_scales", torch.float32)
     _decode("pkv_paged_decode_int8", out, query, k_codes, v_codes, k_scales, v_scales,
+            block_tables, context_lens, max_context_len, softmax_scale, workspace, dev_status,
+            stream)
+
+
+def pkv_paged_decode_fp8(out, query, k_codes, v_codes, k_scales, v_scales, block_tables,
+                         context_lens, max_context_len, softmax_scale, workspace,
+                         dev_status=None, stream=None) -> None:
+    """out[N][Hq][d] fp32 = decode attention of query over FP8 (E4M3) pools."""
+    import torch
+    _check(k_codes, "k_codes", torch.uint8)
+    _check(v_codes, "v_codes", torch.uint8)
+    _check(k_scales, "k_scales", torch.float32)
+    _check(v_scales, "v_scales", torch.float32)
+    _decode("pkv_paged_decode_fp8", out, query, k_codes, v_codes, k_scales, v_scales,
             block_tables, context_lens, max_context_len, softmax_scale, workspace, dev_status,
             stream)
 

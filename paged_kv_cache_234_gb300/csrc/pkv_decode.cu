@@ -32,6 +32,8 @@
 //   S^T[16 tok][8 heads] = K_page[16 x d] . Q^T      (m16n8k16, f16 -> f32)
 //   online softmax in base 2, one update per stage
 //   O^T[d][8 heads]     += V_page^T[d x 16] . P^T    (m16n8k16, f16 -> f32)
+// FP8 (OCP E4M3) codes are widened to f16 exactly by cvt.rn.f16x2.e4m3x2; the
+// K and V scales apply as for INT8.
 // INT8 codes are widened to f16 exactly by byte permutes: a code c placed
 // under the exponent byte 0x64 reads as 1152 + c.  For K the constant 1152
 // is left in and removed from the scores as 1152 * sum(q); for V it is
@@ -112,31 +114,40 @@ struct Tune {
     static constexpr int kMinCtas = kMinCtas_;
 };
 
-template <bool kInt8, int kD>
+// KV kinds: 0 fp16 values; 1 INT8 codes, 2 FP8 (E4M3) codes, both one byte
+// per value with an fp32 K and V scale per (block, kv head).
+constexpr int kKvF16 = 0, kKvI8 = 1, kKvF8 = 2;
+
+template <int kKv, int kD>
 struct TuneOf;
 template <>
-struct TuneOf<false, 128> : Tune<PKV_F16_D128_PPS, PKV_F16_D128_STAGES, PKV_F16_D128_CTAS> {};
+struct TuneOf<kKvF16, 128> : Tune<PKV_F16_D128_PPS, PKV_F16_D128_STAGES, PKV_F16_D128_CTAS> {};
 template <>
-struct TuneOf<true, 128> : Tune<PKV_I8_D128_PPS, PKV_I8_D128_STAGES, PKV_I8_D128_CTAS> {};
+struct TuneOf<kKvI8, 128> : Tune<PKV_I8_D128_PPS, PKV_I8_D128_STAGES, PKV_I8_D128_CTAS> {};
 template <>
-struct TuneOf<false, 64> : Tune<1, 3, 4> {};
+struct TuneOf<kKvF8, 128> : Tune<PKV_I8_D128_PPS, PKV_I8_D128_STAGES, PKV_I8_D128_CTAS> {};
 template <>
-struct TuneOf<true, 64> : Tune<2, 3, 4> {};
+struct TuneOf<kKvF16, 64> : Tune<1, 3, 4> {};
+template <>
+struct TuneOf<kKvI8, 64> : Tune<2, 3, 4> {};
+template <>
+struct TuneOf<kKvF8, 64> : Tune<2, 3, 4> {};
 
-template <bool kInt8, int kD>
+template <int kKv, int kD>
 struct Cfg {
+    static constexpr bool kInt8 = kKv != kKvF16;  // one-byte codes with scales
     static constexpr int kElem = kInt8 ? 1 : 2;
     static constexpr int kRowBytes = kD * kElem;                 // 256 / 128 / 64
     static constexpr int kTileBytes = kPage * kRowBytes;         // one (block, kv head) tile
     static constexpr int kPageBytes = 2 * kTileBytes;            // K tile + V tile
-    static constexpr int kPPS = TuneOf<kInt8, kD>::kPPS;         // pages per stage
+    static constexpr int kPPS = TuneOf<kKv, kD>::kPPS;           // pages per stage
     static constexpr int kStageBytes = kPPS * kPageBytes;
     static constexpr int kBoxInner = kRowBytes > 128 ? 128 / kElem : kD;  // elements
     static constexpr int kBoxes = kD / kBoxInner;
     static constexpr int kBoxBytes = kPage * kBoxInner * kElem;
     static constexpr int kSwizzle = kRowBytes >= 128 ? 128 : 64;
-    static constexpr int kStages = TuneOf<kInt8, kD>::kStages;
-    static constexpr int kMinCtas = TuneOf<kInt8, kD>::kMinCtas;
+    static constexpr int kStages = TuneOf<kKv, kD>::kStages;
+    static constexpr int kMinCtas = TuneOf<kKv, kD>::kMinCtas;
     static_assert(kPPS == 1 || kPPS == 2, "one or two pages per stage");
     static constexpr int kHdrBytes = 32;  // per stage: bad[2], k scale[2], v scale[2]
     static constexpr int kStageRegion = kWarps * kStages * kStageBytes;
@@ -297,11 +308,12 @@ __device__ __forceinline__ void write_split(const DecodeArgs &p, int w, bool val
 }
 
 // S^T fragment (rows: tokens g, g+8; cols: heads 2c, 2c+1) of one page.
-template <bool kInt8, int kD>
+template <int kKv, int kD>
 __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD / 16][2],
                                             int lane, float (&s)[4])
 {
-    using C = Cfg<kInt8, kD>;
+    using C = Cfg<kKv, kD>;
+    constexpr bool kInt8 = C::kInt8;
     constexpr int KS = kD / 16;
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
     if constexpr (!kInt8) {
@@ -323,22 +335,32 @@ __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD
         constexpr int CH = kD / 64;  // 16-byte chunks per row per lane
         uint32_t kw[2][4 * CH];
 #pragma unroll
+        // INT8: flip the sign bit for the biased widening; FP8: as stored
+        constexpr uint32_t kFlip = kKv == kKvI8 ? 0x80808080u : 0u;
         for (int r = 0; r < 2; ++r) {
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
                 const uint4 v = ptx::lds128(kt + swz<C::kRowBytes>(g + 8 * r, CH * c + j));
-                kw[r][4 * j + 0] = v.x ^ 0x80808080u;
-                kw[r][4 * j + 1] = v.y ^ 0x80808080u;
-                kw[r][4 * j + 2] = v.z ^ 0x80808080u;
-                kw[r][4 * j + 3] = v.w ^ 0x80808080u;
+                kw[r][4 * j + 0] = v.x ^ kFlip;
+                kw[r][4 * j + 1] = v.y ^ kFlip;
+                kw[r][4 * j + 2] = v.z ^ kFlip;
+                kw[r][4 * j + 3] = v.w ^ kFlip;
             }
         }
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            const uint32_t a0 = i8pair_biased(kw[0][ks], 0x4140u);
-            const uint32_t a2 = i8pair_biased(kw[0][ks], 0x4342u);
-            const uint32_t a1 = i8pair_biased(kw[1][ks], 0x4140u);
-            const uint32_t a3 = i8pair_biased(kw[1][ks], 0x4342u);
+            uint32_t a0, a1, a2, a3;
+            if constexpr (kKv == kKvI8) {
+                a0 = i8pair_biased(kw[0][ks], 0x4140u);
+                a2 = i8pair_biased(kw[0][ks], 0x4342u);
+                a1 = i8pair_biased(kw[1][ks], 0x4140u);
+                a3 = i8pair_biased(kw[1][ks], 0x4342u);
+            } else {
+                a0 = ptx::e4m3x2_to_f16x2(kw[0][ks]);
+                a2 = ptx::e4m3x2_to_f16x2(kw[0][ks] >> 16);
+                a1 = ptx::e4m3x2_to_f16x2(kw[1][ks]);
+                a3 = ptx::e4m3x2_to_f16x2(kw[1][ks] >> 16);
+            }
             if (ks & 1)
                 ptx::mma_16816(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             else
@@ -350,11 +372,12 @@ __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD
 }
 
 // O^T += V_page^T . P^T for one page; tokens >= ntok contribute nothing.
-template <bool kInt8, int kD>
+template <int kKv, int kD>
 __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1, int ntok,
                                         int lane, float (&o)[kD / 16][4])
 {
-    using C = Cfg<kInt8, kD>;
+    using C = Cfg<kKv, kD>;
+    constexpr bool kInt8 = C::kInt8;
     constexpr int KS = kD / 16;
     const int g = lane >> 2, c = lane & 3;
     if constexpr (!kInt8) {
@@ -374,39 +397,56 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
     } else {
         // lane (g, c): tokens 2c, 2c+1, 2c+8, 2c+9; bytes [DG*g, DG*g + DG), DG = kD/8
         constexpr int NW = kD / 32;  // words per token per lane
+        constexpr uint32_t kFlip = kKv == kKvI8 ? 0x80808080u : 0u;
         uint32_t vw[4][NW];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = 2 * c + (r & 1) + 8 * (r >> 1);
             if constexpr (kD == 128) {
                 const uint4 v = ptx::lds128(vt + swz<C::kRowBytes>(t, g));
-                vw[r][0] = v.x ^ 0x80808080u;
-                vw[r][1] = v.y ^ 0x80808080u;
-                vw[r][2] = v.z ^ 0x80808080u;
-                vw[r][3] = v.w ^ 0x80808080u;
+                vw[r][0] = v.x ^ kFlip;
+                vw[r][1] = v.y ^ kFlip;
+                vw[r][2] = v.z ^ kFlip;
+                vw[r][3] = v.w ^ kFlip;
             } else {
                 const uint2 v = ptx::lds64(vt + swz<C::kRowBytes>(t, g >> 1) + (g & 1) * 8);
-                vw[r][0] = v.x ^ 0x80808080u;
-                vw[r][1] = v.y ^ 0x80808080u;
+                vw[r][0] = v.x ^ kFlip;
+                vw[r][1] = v.y ^ kFlip;
             }
+        }
+        // FP8: rows of tokens past the end are zeroed (a NaN byte there
+        // would survive a zero probability); INT8 codes are always finite
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (kKv == kKvF8 && ntok < kPage) {
+            mlo = (2 * c < ntok ? 0x0000ffffu : 0u) | (2 * c + 1 < ntok ? 0xffff0000u : 0u);
+            mhi = (2 * c + 8 < ntok ? 0x0000ffffu : 0u) | (2 * c + 9 < ntok ? 0xffff0000u : 0u);
         }
 #pragma unroll
         for (int i = 0; i < KS; ++i) {
             const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
             const uint32_t il01 = ptx::prmt(vw[0][i >> 1], vw[1][i >> 1], sel);
             const uint32_t il23 = ptx::prmt(vw[2][i >> 1], vw[3][i >> 1], sel);
-            ptx::mma_16816(o[i], i8pair_exact(il01, 0x4140u), i8pair_exact(il01, 0x4342u),
-                           i8pair_exact(il23, 0x4140u), i8pair_exact(il23, 0x4342u), pb0, pb1);
+            if constexpr (kKv == kKvI8) {
+                ptx::mma_16816(o[i], i8pair_exact(il01, 0x4140u), i8pair_exact(il01, 0x4342u),
+                               i8pair_exact(il23, 0x4140u), i8pair_exact(il23, 0x4342u), pb0,
+                               pb1);
+            } else {
+                ptx::mma_16816(o[i], ptx::e4m3x2_to_f16x2(il01) & mlo,
+                               ptx::e4m3x2_to_f16x2(il01 >> 16) & mlo,
+                               ptx::e4m3x2_to_f16x2(il23) & mhi,
+                               ptx::e4m3x2_to_f16x2(il23 >> 16) & mhi, pb0, pb1);
+            }
         }
     }
 }
 
-template <bool kInt8, int kD>
-__global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
+template <int kKv, int kD>
+__global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv)
 {
-    using C = Cfg<kInt8, kD>;
+    using C = Cfg<kKv, kD>;
+    constexpr bool kInt8 = C::kInt8;
     constexpr int S = C::kStages;
     constexpr int PPS = C::kPPS;
     constexpr int KS = kD / 16;  // mma k-steps over head_dim, also m-tiles of O^T
@@ -584,8 +624,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
                 // sum over the head's four lanes, then fetch heads 2c and 2c+1
                 qs += __shfl_xor_sync(0xffffffffu, qs, 1);
                 qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-                qb0 = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c);
-                qb1 = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
+                if constexpr (kKv == kKvI8) {  // FP8 codes carry no bias
+                    qb0 = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c);
+                    qb1 = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
+                }
             } else {
                 const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
 #pragma unroll
@@ -635,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
             for (int u = 0; u < PPS; ++u) {
                 if (good[u]) {
                     float sc[4];
-                    page_scores<kInt8, kD>(st + u * C::kPageBytes, qf, lane, sc);
+                    page_scores<kKv, kD>(st + u * C::kPageBytes, qf, lane, sc);
                     float sl = p.scale_log2;
                     if constexpr (kInt8) {
                         sl *= hf[2 + u];
@@ -707,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kInt8, kD>::kMinCtas)
                     const uint32_t pb1 =
                         ptx::movmatrix_t(pack_half2(pr[u][2] * sv, pr[u][3] * sv));
                     const int ntok = min(kPage, ctx - (cc.page + u) * kPage);
-                    page_pv<kInt8, kD>(st + u * C::kPageBytes + C::kTileBytes, pb0, pb1, ntok,
+                    page_pv<kKv, kD>(st + u * C::kPageBytes + C::kTileBytes, pb0, pb1, ntok,
                                        lane, o);
                 }
             }
@@ -1013,15 +1055,15 @@ struct OccCache {
     int per_sm = 0;
 };
 
-template <bool kInt8, int kD>
+template <int kKv, int kD>
 pkv_status launch(const DecodeCall &call, const Shape &sh)
 {
-    using C = Cfg<kInt8, kD>;
+    using C = Cfg<kKv, kD>;
     DeviceInfo di;
     if (!current_device_info(&di)) return PKV_ERR_CUDA;
     const size_t smem = C::smem_bytes(call.num_seqs);
     if (smem > di.max_smem_optin) return PKV_ERR_UNSUPPORTED;
-    auto kern = decode_kernel<kInt8, kD>;
+    auto kern = decode_kernel<kKv, kD>;
     static OccCache occ[64];
     int per_sm = 0;
     int cap = 0;
@@ -1098,8 +1140,9 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     return PKV_OK;
 }
 
-pkv_status decode_entry(const DecodeCall &call, bool int8)
+pkv_status decode_entry(const DecodeCall &call, int kv)
 {
+    const bool int8 = kv != kKvF16;
     if (!call.out || !call.query || !call.kpool || !call.vpool || !call.block_tables ||
         !call.context_lens)
         return PKV_ERR_INVALID_ARG;
@@ -1126,10 +1169,11 @@ pkv_status decode_entry(const DecodeCall &call, bool int8)
     const size_t need = workspace_bytes_for(sh, call.head_dim);
     if (need > 0 && (!call.workspace || call.workspace_bytes < need)) return PKV_ERR_WORKSPACE;
     if (call.workspace && !aligned(call.workspace, 16)) return PKV_ERR_MISALIGNED;
-    if (int8) {
-        return call.head_dim == 128 ? launch<true, 128>(call, sh) : launch<true, 64>(call, sh);
-    }
-    return call.head_dim == 128 ? launch<false, 128>(call, sh) : launch<false, 64>(call, sh);
+    if (kv == kKvF8)
+        return call.head_dim == 128 ? launch<kKvF8, 128>(call, sh) : launch<kKvF8, 64>(call, sh);
+    if (kv == kKvI8)
+        return call.head_dim == 128 ? launch<kKvI8, 128>(call, sh) : launch<kKvI8, 64>(call, sh);
+    return call.head_dim == 128 ? launch<kKvF16, 128>(call, sh) : launch<kKvF16, 64>(call, sh);
 }
 
 }  // namespace
@@ -1148,7 +1192,7 @@ extern "C" pkv_status pkv_paged_decode_fp16(float *out, const void *query, const
                                block_tables, max_blocks_per_seq, context_lens, max_context_len,
                                num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                softmax_scale, workspace, workspace_bytes, dev_status, stream};
-    return pkv::decode_entry(call, false);
+    return pkv::decode_entry(call, pkv::kKvF16);
 }
 
 extern "C" pkv_status pkv_paged_decode_int8(float *out, const void *query, const int8_t *k_codes,
@@ -1165,7 +1209,24 @@ extern "C" pkv_status pkv_paged_decode_int8(float *out, const void *query, const
                                block_tables, max_blocks_per_seq, context_lens, max_context_len,
                                num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                softmax_scale, workspace, workspace_bytes, dev_status, stream};
-    return pkv::decode_entry(call, true);
+    return pkv::decode_entry(call, pkv::kKvI8);
+}
+
+extern "C" pkv_status pkv_paged_decode_fp8(float *out, const void *query, const uint8_t *k_codes,
+                                           const uint8_t *v_codes, const float *k_scales,
+                                           const float *v_scales, int num_blocks,
+                                           const int32_t *block_tables, int max_blocks_per_seq,
+                                           const int32_t *context_lens, int max_context_len,
+                                           int num_seqs, int num_heads, int num_kv_heads,
+                                           int head_dim, int block_size, float softmax_scale,
+                                           void *workspace, size_t workspace_bytes,
+                                           int32_t *dev_status, void *stream)
+{
+    const pkv::DecodeCall call{out, query, k_codes, v_codes, k_scales, v_scales, num_blocks,
+                               block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                               num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                               softmax_scale, workspace, workspace_bytes, dev_status, stream};
+    return pkv::decode_entry(call, pkv::kKvF8);
 }
 
 extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
@@ -1233,5 +1294,5 @@ extern "C" pkv_status pkv_paged_decode_int8_static_workspace(
                                softmax_scale, ws, PKV_STATIC_WORKSPACE_BYTES, dev_status, stream};
     // a call needing more than PKV_STATIC_WORKSPACE_BYTES of scratch is
     // rejected with PKV_ERR_WORKSPACE before anything is launched
-    return pkv::decode_entry(call, true);
+    return pkv::decode_entry(call, pkv::kKvI8);
 }

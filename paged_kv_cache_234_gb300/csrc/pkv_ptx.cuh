@@ -192,6 +192,16 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
     return d;
 }
 
+// Two OCP E4M3 values (the low 16 bits of w, low byte first) to an f16 pair
+// (low byte -> low half); exact, every E4M3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w)
+{
+    uint32_t r;
+    const unsigned short h = static_cast<unsigned short>(w & 0xffffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+    return r;
+}
+
 __device__ __forceinline__ void griddep_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");

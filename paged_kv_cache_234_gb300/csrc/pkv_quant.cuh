@@ -6,10 +6,12 @@
 // A 128-thread CTA owns one tile; thread `tid` holds the 16-byte chunks
 // c * 128 + tid (c < kChunks) as raw fp16 bits.  amax = max |x| (NaN
 // ignored), scale = fl32(amax / 127), code = round-half-even(fl32(x / scale))
-// clamped to [-127, 127], a NaN quotient giving 0.
+// clamped to [-127, 127], a NaN quotient giving 0; for FP8 (E4M3) codes the
+// same with 448 and the nearest E4M3 value of the quotient.
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace pkv {
@@ -88,6 +90,31 @@ __device__ __forceinline__ uint2 chunk_codes(const uint4 &raw, float scale, floa
         const uint32_t b2 = static_cast<uint32_t>(quant_code(f1.x, scale, rcp)) & 0xffu;
         const uint32_t b3 = static_cast<uint32_t>(quant_code(f1.y, scale, rcp)) & 0xffu;
         packed[w] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+    return make_uint2(packed[0], packed[1]);
+}
+
+// FP8 (OCP E4M3) code of x: the IEEE fp32 quotient x / scale rounded to the
+// nearest E4M3 value (ties to even), saturated to +-448; a NaN quotient (0/0,
+// inf/inf, NaN input) gives code 0.
+__device__ __forceinline__ uint32_t fp8_code(float x, float scale)
+{
+    const float y = __fdiv_rn(x, scale);
+    if (isnan(y)) return 0u;
+    return static_cast<uint32_t>(__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Eight FP8 codes of one 16-byte chunk, packed little-endian into a uint2.
+__device__ __forceinline__ uint2 chunk_codes_fp8(const uint4 &raw, float scale)
+{
+    const __half2 *hp = reinterpret_cast<const __half2 *>(&raw);
+    uint32_t packed[2];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const float2 f0 = __half22float2(hp[2 * w]);
+        const float2 f1 = __half22float2(hp[2 * w + 1]);
+        packed[w] = fp8_code(f0.x, scale) | (fp8_code(f0.y, scale) << 8) |
+                    (fp8_code(f1.x, scale) << 16) | (fp8_code(f1.y, scale) << 24);
     }
     return make_uint2(packed[0], packed[1]);
 }

@@ -1,6 +1,8 @@
 // pkv_quantize.cu -- symmetric per-(block, kv head) INT8 quantization of fp16
 // K and V tiles (PagedKV-Fusion README, "Overview" component B and the
-// "Architecture" sequence diagram step "INT8 survivors + scales").
+// "Architecture" sequence diagram step "INT8 survivors + scales"), and the
+// same with FP8 (OCP E4M3) codes and scale = amax / 448 ("PagedAttention &
+// KV-Cache Memory Management", section 5.1: per-block scaled FP8 KV).
 //
 // One 128-thread CTA per (block, kv head, K|V) tile of 16 x head_dim fp16
 // values (grid-strided when there are many tiles).  The tile is read once with
@@ -20,10 +22,10 @@
 namespace pkv {
 namespace {
 
-template <int kHeadDim>
+template <int kHeadDim, bool kFp8>
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_kernel(const __half *__restrict__ k_in, const __half *__restrict__ v_in,
-                    int8_t *__restrict__ k_out, int8_t *__restrict__ v_out,
+                    uint8_t *__restrict__ k_out, uint8_t *__restrict__ v_out,
                     float *__restrict__ k_scales, float *__restrict__ v_scales,
                     const int32_t *__restrict__ block_ids, int64_t tiles_per_pool,
                     int num_kv_heads, int num_blocks, int32_t *dev_status)
@@ -56,12 +58,13 @@ __global__ void __launch_bounds__(kQuantThreads)
         for (int c = 0; c < kChunks; ++c) raw[c] = __ldcs(src + c * kQuantThreads + threadIdx.x);
 
         const float amax = cta_absmax(chunks_absmax(raw), warp_max);
-        const float scale = __fdiv_rn(amax, 127.0f);
+        const float scale = __fdiv_rn(amax, kFp8 ? 448.0f : 127.0f);
         const float rcp = __frcp_rn(scale);
 
 #pragma unroll
         for (int c = 0; c < kChunks; ++c)
-            __stcs(dst + c * kQuantThreads + threadIdx.x, chunk_codes(raw[c], scale, rcp));
+            __stcs(dst + c * kQuantThreads + threadIdx.x,
+                   kFp8 ? chunk_codes_fp8(raw[c], scale) : chunk_codes(raw[c], scale, rcp));
         if (threadIdx.x == 0) (is_v ? v_scales : k_scales)[tile] = scale;
     }
 }
@@ -69,13 +72,14 @@ __global__ void __launch_bounds__(kQuantThreads)
 }  // namespace
 }  // namespace pkv
 
-extern "C" pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16, int8_t *k_codes,
-                                          int8_t *v_codes, float *k_scales, float *v_scales,
-                                          const int32_t *block_ids, int num_ids, int num_blocks,
-                                          int num_kv_heads, int head_dim, int block_size,
-                                          int32_t *dev_status, void *stream)
+namespace pkv {
+namespace {
+
+pkv_status quantize_entry(const void *k_fp16, const void *v_fp16, void *k_codes, void *v_codes,
+                          float *k_scales, float *v_scales, const int32_t *block_ids,
+                          int num_ids, int num_blocks, int num_kv_heads, int head_dim,
+                          int block_size, int32_t *dev_status, void *stream, bool fp8)
 {
-    using namespace pkv;
     if (!k_fp16 || !v_fp16 || !k_codes || !v_codes || !k_scales || !v_scales)
         return PKV_ERR_INVALID_ARG;
     if (num_blocks <= 0 || num_kv_heads <= 0 || num_ids < 0 || head_dim <= 0 || block_size <= 0)
@@ -107,15 +111,51 @@ extern "C" pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16
     cfg.numAttrs = 1;
     const __half *kin = static_cast<const __half *>(k_fp16);
     const __half *vin = static_cast<const __half *>(v_fp16);
-    const cudaError_t e =
-        head_dim == 128
-            ? cudaLaunchKernelEx(&cfg, quantize_kernel<128>, kin, vin, k_codes, v_codes, k_scales,
-                                 v_scales, block_ids, tiles, num_kv_heads, num_blocks, dev_status)
-            : cudaLaunchKernelEx(&cfg, quantize_kernel<64>, kin, vin, k_codes, v_codes, k_scales,
-                                 v_scales, block_ids, tiles, num_kv_heads, num_blocks, dev_status);
+    uint8_t *kc = static_cast<uint8_t *>(k_codes), *vc = static_cast<uint8_t *>(v_codes);
+    cudaError_t e;
+    if (head_dim == 128)
+        e = fp8 ? cudaLaunchKernelEx(&cfg, quantize_kernel<128, true>, kin, vin, kc, vc, k_scales,
+                                     v_scales, block_ids, tiles, num_kv_heads, num_blocks,
+                                     dev_status)
+                : cudaLaunchKernelEx(&cfg, quantize_kernel<128, false>, kin, vin, kc, vc,
+                                     k_scales, v_scales, block_ids, tiles, num_kv_heads,
+                                     num_blocks, dev_status);
+    else
+        e = fp8 ? cudaLaunchKernelEx(&cfg, quantize_kernel<64, true>, kin, vin, kc, vc, k_scales,
+                                     v_scales, block_ids, tiles, num_kv_heads, num_blocks,
+                                     dev_status)
+                : cudaLaunchKernelEx(&cfg, quantize_kernel<64, false>, kin, vin, kc, vc,
+                                     k_scales, v_scales, block_ids, tiles, num_kv_heads,
+                                     num_blocks, dev_status);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }
     return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16, int8_t *k_codes,
+                                          int8_t *v_codes, float *k_scales, float *v_scales,
+                                          const int32_t *block_ids, int num_ids, int num_blocks,
+                                          int num_kv_heads, int head_dim, int block_size,
+                                          int32_t *dev_status, void *stream)
+{
+    return pkv::quantize_entry(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, block_ids,
+                               num_ids, num_blocks, num_kv_heads, head_dim, block_size,
+                               dev_status, stream, false);
+}
+
+extern "C" pkv_status pkv_quantize_blocks_fp8(const void *k_fp16, const void *v_fp16,
+                                              uint8_t *k_codes, uint8_t *v_codes,
+                                              float *k_scales, float *v_scales,
+                                              const int32_t *block_ids, int num_ids,
+                                              int num_blocks, int num_kv_heads, int head_dim,
+                                              int block_size, int32_t *dev_status, void *stream)
+{
+    return pkv::quantize_entry(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, block_ids,
+                               num_ids, num_blocks, num_kv_heads, head_dim, block_size,
+                               dev_status, stream, true);
 }

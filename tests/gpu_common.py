@@ -29,10 +29,11 @@ def dev(a, dtype=None):
     return t.cuda()
 
 
-def oracle_codes(w):
-    """INT8 pools + scales from the oracle quantizer (used blocks only)."""
-    kc, ks = oracle.quantize(w.k_pool, block_ids=w.used_block_ids)
-    vc, vs = oracle.quantize(w.v_pool, block_ids=w.used_block_ids)
+def oracle_codes(w, fp8=False):
+    """INT8 (or FP8) pools + scales from the oracle quantizer (used blocks only)."""
+    q = oracle.quantize_fp8 if fp8 else oracle.quantize
+    kc, ks = q(w.k_pool, block_ids=w.used_block_ids)
+    vc, vs = q(w.v_pool, block_ids=w.used_block_ids)
     return kc, vc, ks, vs
 
 
@@ -52,9 +53,10 @@ def gpu_decode(w, variant, codes=None, max_context_len=None, tables=None, lens=N
         pkv.pkv_paged_decode_fp16(out, q, dev(w.k_pool), dev(w.v_pool), bt, cl, mcl,
                                   w.softmax_scale, ws, status, stream=stream)
     else:
-        kc, vc, ks, vs = codes if codes is not None else oracle_codes(w)
-        pkv.pkv_paged_decode_int8(out, q, dev(kc), dev(vc), dev(ks), dev(vs), bt, cl, mcl,
-                                  w.softmax_scale, ws, status, stream=stream)
+        kc, vc, ks, vs = codes if codes is not None else oracle_codes(w, variant == "fp8")
+        fn = pkv.pkv_paged_decode_fp8 if variant == "fp8" else pkv.pkv_paged_decode_int8
+        fn(out, q, dev(kc), dev(vc), dev(ks), dev(vs), bt, cl, mcl, w.softmax_scale, ws, status,
+           stream=stream)
     torch.cuda.synchronize()
     return out.cpu().numpy().astype(np.float64), int(status.item())
 
@@ -67,10 +69,10 @@ def oracle_decode(w, variant, codes=None, max_context_len=None, tables=None, len
         return oracle.decode_fp16(w.query, w.k_pool, w.v_pool, bt, cl,
                                   num_kv_heads=w.num_kv_heads, softmax_scale=w.softmax_scale,
                                   max_context_len=mcl, return_flags=True)
-    kc, vc, ks, vs = codes if codes is not None else oracle_codes(w)
-    return oracle.decode_int8(w.query, kc, vc, ks, vs, bt, cl, num_kv_heads=w.num_kv_heads,
-                              softmax_scale=w.softmax_scale, max_context_len=mcl,
-                              return_flags=True)
+    kc, vc, ks, vs = codes if codes is not None else oracle_codes(w, variant == "fp8")
+    fn = oracle.decode_fp8 if variant == "fp8" else oracle.decode_int8
+    return fn(w.query, kc, vc, ks, vs, bt, cl, num_kv_heads=w.num_kv_heads,
+              softmax_scale=w.softmax_scale, max_context_len=mcl, return_flags=True)
 
 
 def assert_close(got, ref, what=""):

@@ -15,27 +15,28 @@ from gpu_common import (assert_close, dev, ensure_built, gpu_decode, oracle_code
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["fp16", "int8"]
+VARIANTS = ["fp16", "int8", "fp8"]
 _cache = {}
 
 
-def workload(name):
+def workload(name, variant):
     if name not in _cache:
-        w = W.make(name)
-        _cache[name] = (w, oracle_codes(w))
-    return _cache[name]
+        _cache.clear()  # one configuration at a time (the full-size pools are large)
+        _cache[name] = (W.make(name), {})
+    w, codes = _cache[name]
+    if variant != "fp16" and variant not in codes:
+        codes[variant] = oracle_codes(w, variant == "fp8")
+    return w, codes.get(variant)
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("name", W.CONFIG_NAMES)
 def test_configs_match_oracle(name, variant):
-    w, codes = workload(name)
+    w, codes = workload(name, variant)
     got, st = gpu_decode(w, variant, codes)
     ref, flags = oracle_decode(w, variant, codes)
     assert st == 0 and not flags.any()
     assert_close(got, ref, f"{name}/{variant}")
-    if name in ("c5a_64x2048", "c5b_256_ragged"):
-        _cache.pop(name)
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -45,7 +46,7 @@ def test_split_count_sweep(variant, workers):
     # oracle's answer, and to each other within float rounding
     w = W.random_case(40, num_seqs=6, num_heads=8, num_kv_heads=2, head_dim=128,
                       context_lens=[300, 1, 77, 512, 16, 250])
-    codes = oracle_codes(w)
+    codes = oracle_codes(w, variant == "fp8")
     ensure_built()
     try:
         pkv.pkv_set_decode_workers(workers)
@@ -68,7 +69,7 @@ def test_group_sizes_and_edge_lengths(variant, hq, hkv, d):
     lens = [1, 15, 16, 17, 0, 33, 255, 256, 257]
     w = W.random_case(7 * hq + d, num_seqs=len(lens), num_heads=hq, num_kv_heads=hkv,
                       head_dim=d, context_lens=lens)
-    codes = oracle_codes(w)
+    codes = oracle_codes(w, variant == "fp8")
     got, st = gpu_decode(w, variant, codes)
     ref, flags = oracle_decode(w, variant, codes)
     assert st == 0 and not flags.any()
@@ -80,7 +81,7 @@ def test_group_sizes_and_edge_lengths(variant, hq, hkv, d):
 def test_bad_block_id_and_bad_length_give_zeros_and_status(variant):
     w = W.random_case(55, num_seqs=5, num_heads=8, num_kv_heads=2, head_dim=64,
                       context_lens=[40, 100, 64, 5, 70])
-    codes = oracle_codes(w)
+    codes = oracle_codes(w, variant == "fp8")
     tables = w.block_tables.copy()
     tables[1, 3] = w.num_blocks + 1000   # out of the pool, inside the context
     tables[4, 2] = -7
@@ -97,7 +98,7 @@ def test_bad_block_id_and_bad_length_give_zeros_and_status(variant):
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_side_stream_and_determinism(variant):
     w = W.random_case(66, num_seqs=12, num_heads=32, num_kv_heads=8, head_dim=128, max_ctx=700)
-    codes = oracle_codes(w)
+    codes = oracle_codes(w, variant == "fp8")
     s = torch.cuda.Stream()
     a, _ = gpu_decode(w, variant, codes, stream=s)
     b, _ = gpu_decode(w, variant, codes, stream=s)

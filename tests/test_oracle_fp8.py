@@ -49,6 +49,20 @@ def test_rounding_matches_torch():
     assert bad.size == 0, [(float(vals[i]), int(got[i]), int(ref[i])) for i in bad[:5]]
 
 
+# The encoder against a brute-force search over all finite codes (nearest
+# value, ties to the code with an even last bit) on a dense sweep.
+def test_rounding_matches_brute_force_search():
+    lut = np.array([oracle.e4m3_to_double(c) for c in range(0x7F)])
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([rng.uniform(0, 470, 3000), rng.uniform(0, 0.05, 2000),
+                           (lut[:-1] + lut[1:]) / 2, lut]).astype(np.float32)
+    for v in vals:
+        err = np.abs(lut - float(v))
+        best = np.flatnonzero(err == err.min())
+        want = best[0] if best.size == 1 else [b for b in best if b % 2 == 0][0]
+        assert oracle.e4m3_from_float(float(v)) == want, float(v)
+
+
 def test_saturation_beyond_the_largest_finite_value():
     for v in (448.0, 449.0, 463.99, 464.0, 470.0, 1e6, 3.0e38):
         assert oracle.e4m3_from_float(v) == 0x7E
