@@ -47,7 +47,7 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2: written, then another one read, between 
 # DRAM bytes per launch of the INT8 decode (decode + reduce kernels) on this
 # workload from the ncu capture summarised in profiles/, with the hash of the
 # kernel source it was taken on; the figure is dropped when the source changes.
-TRAFFIC = {"decode_int8": (273772800 + 5041408, "856376e9957a373a")}  # decode + reduce kernels
+TRAFFIC = {"decode_int8": (273446144 + 5041152, "187f4f9adbae7fd0")}  # decode + reduce kernels
 
 
 def _src_hash():
@@ -344,6 +344,74 @@ def run_profile_small(args):
     print(f"profile run: {args.profile} x{args.warmup + args.steps}", flush=True)
 
 
+def run_report(args):
+    """Per configuration and variant: p50 / p90 us per decode call over 200
+    timed calls after 20 warm-ups, L2 flushed before each call; KV GB/s of
+    the logical bytes (unique bytes too where sequences share blocks) and
+    sequence-steps/s.  One JSON line per (configuration, variant)."""
+    import torch
+    import paged_kv_cache_234_gb300 as pkv
+    from paged_kv_cache_234_gb300 import build as pkv_build
+    pkv_build.build()
+    peak, _ = _peaks()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    fw = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    fr = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for name in W.CONFIG_NAMES:
+        w = W.make(name)
+        n, hq, d = w.query.shape
+        hkv = w.num_kv_heads
+        kf, vf = dev(w.k_pool), dev(w.v_pool)
+        q, bt, cl = dev(w.query), dev(w.block_tables), dev(w.context_lens)
+        used = dev(w.used_block_ids)
+        out = torch.empty((n, hq, d), dtype=torch.float32, device="cuda")
+        ws_t = pkv.decode_workspace(n, hq, hkv, d, w.max_context_len)
+        pools = {}
+        for kind, qfn, dt in (("int8", pkv.pkv_quantize_blocks, torch.int8),
+                              ("fp8", pkv.pkv_quantize_blocks_fp8, torch.uint8)):
+            kc = torch.zeros(w.k_pool.shape, dtype=dt, device="cuda")
+            vc = torch.zeros_like(kc)
+            ks = torch.zeros(w.k_pool.shape[:2], dtype=torch.float32, device="cuda")
+            vs = torch.zeros_like(ks)
+            qfn(kf, vf, kc, vc, ks, vs, used)
+            pools[kind] = (kc, vc, ks, vs)
+        calls = {
+            "fp16": lambda: pkv.pkv_paged_decode_fp16(out, q, kf, vf, bt, cl, w.max_context_len,
+                                                      w.softmax_scale, ws_t),
+            "int8": lambda: pkv.pkv_paged_decode_int8(out, q, *pools["int8"], bt, cl,
+                                                      w.max_context_len, w.softmax_scale, ws_t),
+            "fp8": lambda: pkv.pkv_paged_decode_fp8(out, q, *pools["fp8"], bt, cl,
+                                                    w.max_context_len, w.softmax_scale, ws_t),
+        }
+        # blocks read once per call when sequences share them (c4: shared prefix)
+        uniq_ctx = np.full(w.used_block_ids.size, 16, np.int64)
+        for variant, fn in calls.items():
+            for _ in range(20):
+                fn()
+            ts = []
+            for _ in range(200):
+                fw.zero_()
+                fr.view(torch.int32).max()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+            eb, sc = (2, False) if variant == "fp16" else (1, True)
+            b = decode_bytes(w.context_lens, hkv, d, eb, sc)
+            bu = decode_bytes(uniq_ctx, hkv, d, eb, sc)
+            t50, t90 = statistics.median(ts), float(np.percentile(ts, 90))
+            print(json.dumps({"config": name, "variant": variant, "p50_us": 1e6 * t50,
+                              "p90_us": 1e6 * t90, "kv_bytes": b, "unique_kv_bytes": bu,
+                              "GB/s": b / t50 / 1e9, "frac_of_peak": b / t50 / 1e9 / peak,
+                              "seq_steps_per_s": n / t50}), flush=True)
+        del kf, vf, pools
+        torch.cuda.empty_cache()
+
+
 def evict_cpu_us(num_blocks, reps=20):
     """The oracle's eviction (scores + sort-based choice) on this host."""
     import oracle
@@ -365,6 +433,9 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--report-configs", action="store_true",
+                    help="p50/p90 of every decode variant on every configuration, one JSON "
+                         "line each (no benchmark line)")
     ap.add_argument("--profile", choices=["int8", "fp8", "fp16", "quantize", "append", "evict"],
                     help="profiling run: the same batch over a 16384-block pool (eviction: "
                          "a 65536-block pool), only warm-up + timed calls of one kernel, "
@@ -373,6 +444,9 @@ def main():
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+        return
+    if args.report_configs:
+        run_report(args)
         return
     if args.profile in ("append", "evict"):
         run_profile_small(args)
