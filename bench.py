@@ -619,12 +619,22 @@ def main():
             evict[str(nb_e)]["cpu_oracle_p50_us"] = evict_cpu_us(nb_e)
 
     # end to end through the public API with host buffers: per step the
-    # query, block tables, context lengths and tail ids go host -> device and
-    # the output comes back
-    hq_pin = torch.from_numpy(w.query).pin_memory()
-    hbt_pin = torch.from_numpy(w.block_tables).pin_memory()
-    hcl_pin = torch.from_numpy(w.context_lens).pin_memory()
-    htl_pin = torch.from_numpy(tails_np).pin_memory()
+    # query, block tables, context lengths and tail ids go host -> device in
+    # one copy (one pinned staging buffer, the device inputs are views of its
+    # device twin, as a serving loop would stage them) and the output comes
+    # back
+    parts = [w.query, w.block_tables, w.context_lens, tails_np]
+    offs, total_b = [], 0
+    for a in parts:
+        offs.append(total_b)
+        total_b += (a.nbytes + 255) // 256 * 256
+    host_stage = torch.empty(total_b, dtype=torch.uint8).pin_memory()
+    dev_stage = torch.empty(total_b, dtype=torch.uint8, device="cuda")
+    views = []
+    for a, o in zip(parts, offs):
+        host_stage[o:o + a.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)))
+        views.append(dev_stage[o:o + a.nbytes].view(torch.from_numpy(a).dtype).view(a.shape))
+    q_e, bt_e, cl_e, tl_e = views
     hout = torch.empty((n, hq, d), dtype=torch.float32).pin_memory()
     Ke = min(K, 500)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -633,17 +643,16 @@ def main():
     for i in range(Ke):
         l2_flush()
         e0.record(stream)
-        q.copy_(hq_pin, non_blocking=True)
-        bt.copy_(hbt_pin, non_blocking=True)
-        cl.copy_(hcl_pin, non_blocking=True)
-        tails.copy_(htl_pin, non_blocking=True)
-        step_int8()
-        decode_int8()
+        dev_stage.copy_(host_stage, non_blocking=True)
+        pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, tl_e, status)
+        pkv.pkv_paged_decode_int8(out, q_e, kc, vc, ks, vs, bt_e, cl_e, mcl, w.softmax_scale,
+                                  ws_t, status)
         hout.copy_(out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
-    h2d = (w.query.nbytes + w.block_tables.nbytes + w.context_lens.nbytes + tails_np.nbytes)
+    assert torch.equal(hout, out.cpu())
+    h2d = total_b  # the staging buffer copied each step (inputs + alignment padding)
     d2h = n * hq * d * 4
     st_val = int(status.item())
 
