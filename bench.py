@@ -240,7 +240,8 @@ def run_reference(args, ws, rank):
 
 
 def cpu_baseline(w, seconds=10.0):
-    """Oracle INT8 decode on a bounded sample, timed on this host's cores."""
+    """Oracle INT8 decode on a bounded sample, timed on this host's cores:
+    all threads (the reported value) and one thread (reported beside it)."""
     import oracle
     threads = oracle.max_threads()
     seqs = np.arange(4)
@@ -248,19 +249,26 @@ def cpu_baseline(w, seconds=10.0):
     kc, ks = oracle.quantize(kp)
     vc, vs = oracle.quantize(vp)
     nb = decode_bytes(lens, w.num_kv_heads, w.head_dim, 1, True)
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        oracle.decode_int8(w.query[seqs], kc, vc, ks, vs, tab, lens,
-                           num_kv_heads=w.num_kv_heads, softmax_scale=w.softmax_scale,
-                           num_threads=threads)
-        reps += 1
-        dt = time.perf_counter() - t0
-        if dt >= seconds:
-            break
-    return {"value": nb * reps / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+
+    def rate(nthreads, secs):
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.decode_int8(w.query[seqs], kc, vc, ks, vs, tab, lens,
+                               num_kv_heads=w.num_kv_heads, softmax_scale=w.softmax_scale,
+                               num_threads=nthreads)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= secs:
+                return nb * reps / dt / 1e9, reps, dt
+
+    value, reps, dt = rate(threads, seconds)
+    single, reps1, dt1 = rate(1, seconds / 4)
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"fp64 INT8 decode of 4 of {w.num_seqs} sequences, repeated {reps} times "
-                      f"({dt:.1f} s)"}
+                      f"({dt:.1f} s)",
+            "single_thread": {"value": single, "unit": UNIT,
+                              "sample": f"the same, 1 thread, {reps1} times ({dt1:.1f} s)"}}
 
 
 def run_profile(args):

@@ -290,6 +290,19 @@ PKV_API pkv_status pkv_append_int8(void *k_cache, void *v_cache, int8_t *k_codes
                                    void *stream);
 
 /*
+ * pkv_append_fp8 -- pkv_append_int8 for an FP8 (E4M3) cache: the written
+ * tiles are re-quantized as pkv_quantize_blocks_fp8 would (bit-identical).
+ * uint8 code pools; otherwise as pkv_append_int8.
+ */
+PKV_API pkv_status pkv_append_fp8(void *k_cache, void *v_cache, uint8_t *k_codes,
+                                  uint8_t *v_codes, float *k_scales, float *v_scales,
+                                  int num_blocks, const void *k_new, const void *v_new,
+                                  const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *positions, int num_seqs, int num_kv_heads,
+                                  int head_dim, int block_size, int32_t *dev_status,
+                                  void *stream);
+
+/*
  * pkv_evict_select -- score every physical block for eviction and choose
  * the k most evictable ones, in one launch ([PKF] Overview component A
  * "Eviction score: fused scoring + top-k over paged KV blocks", sequence

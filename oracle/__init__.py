@@ -291,6 +291,17 @@ def append_int8(k_pool, v_pool, k_codes, v_codes, k_scales, v_scales, k_new, v_n
     return kp, vp, kc, vc, ks, vs, flags
 
 
+def append_fp8(k_pool, v_pool, k_codes, v_codes, k_scales, v_scales, k_new, v_new,
+               block_tables, positions):
+    """``append_fp16``, then ``quantize_fp8`` of every written tile (other
+    tiles keep their codes and scales)."""
+    kp, vp, flags, written = append_fp16(k_pool, v_pool, k_new, v_new, block_tables, positions)
+    ids = written[written >= 0]
+    kc, ks = quantize_fp8(kp, block_ids=ids, code_pool=k_codes, scales=k_scales)
+    vc, vs = quantize_fp8(vp, block_ids=ids, code_pool=v_codes, scales=v_scales)
+    return kp, vp, kc, vc, ks, vs, flags
+
+
 EVICT_ALPHA = 0.7  # weights of the least-reference-count + age score
 EVICT_BETA = 0.3
 

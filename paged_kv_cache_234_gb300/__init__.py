@@ -47,6 +47,7 @@ PKV_DEV_TIMEOUT = 4
 EXPORTED = ("pkv_quantize_blocks", "pkv_paged_decode_fp16", "pkv_paged_decode_int8",
             "pkv_quantize_blocks_fp8", "pkv_paged_decode_fp8",
             "pkv_paged_decode_int8_static_workspace", "pkv_append_fp16", "pkv_append_int8",
+            "pkv_append_fp8",
             "pkv_evict_select", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_allocate",
             "pkv_bm_free", "pkv_bm_fork", "pkv_bm_cow", "pkv_bm_set_fill", "pkv_bm_stats",
             "pkv_bm_refcounts", "pkv_copy_blocks", "pkv_decode_workspace_size",
@@ -106,6 +107,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_append_fp16.argtypes = app
         L.pkv_append_int8.restype = I
         L.pkv_append_int8.argtypes = app[:2] + [P, P, P, P] + app[2:]
+        L.pkv_append_fp8.restype = I
+        L.pkv_append_fp8.argtypes = app[:2] + [P, P, P, P] + app[2:]
         L.pkv_evict_select.restype = I
         L.pkv_evict_select.argtypes = [P, P, I, ctypes.c_int64, F, F, I, P, P, P, P]
         L.pkv_bm_create.restype = I
@@ -324,8 +327,9 @@ def _append(fn_name, k_cache, v_cache, codes, k_new, v_new, block_tables, positi
     args = [_ptr(k_cache), _ptr(v_cache)]
     if codes is not None:
         kc, vc, ks, vs = codes
-        _check(kc, "k_codes", torch.int8)
-        _check(vc, "v_codes", torch.int8)
+        code_t = torch.uint8 if fn_name.endswith("fp8") else torch.int8
+        _check(kc, "k_codes", code_t)
+        _check(vc, "v_codes", code_t)
         _check(ks, "k_scales", torch.float32)
         _check(vs, "v_scales", torch.float32)
         args += [_ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs)]
@@ -348,6 +352,13 @@ def pkv_append_int8(k_cache, v_cache, k_codes, v_codes, k_scales, v_scales, k_ne
                     block_tables, positions, dev_status=None, stream=None) -> None:
     """pkv_append_fp16, then re-quantize every (block, kv head) tile written."""
     _append("pkv_append_int8", k_cache, v_cache, (k_codes, v_codes, k_scales, v_scales), k_new,
+            v_new, block_tables, positions, dev_status, stream)
+
+
+def pkv_append_fp8(k_cache, v_cache, k_codes, v_codes, k_scales, v_scales, k_new, v_new,
+                   block_tables, positions, dev_status=None, stream=None) -> None:
+    """pkv_append_fp16, then re-quantize every written tile to FP8 (E4M3)."""
+    _append("pkv_append_fp8", k_cache, v_cache, (k_codes, v_codes, k_scales, v_scales), k_new,
             v_new, block_tables, positions, dev_status, stream)
 
 

@@ -8,13 +8,13 @@
 // fp16 cache: one thread per 16-byte chunk of a new row; a row of head_dim
 // fp16 values is 8 or 16 threads, so a warp writes 2 or 4 full rows.
 //
-// INT8 cache: the written (block, kv head) tile is re-quantized in the same
-// kernel.  One 128-thread CTA per (sequence, kv head, K|V) tile reads the 15
-// other rows from the fp16 pool, takes the new row from the input (and writes
-// it to the fp16 pool), then quantizes the tile exactly as the quantize
-// kernel does: bit-identical codes and scale to quantizing the tile after a
-// plain fp16 append.  Latency-bound for a decode batch: 4 KiB read and
-// about 2.3 KiB written per tile at head_dim 128.
+// INT8 (or FP8 E4M3) cache: the written (block, kv head) tile is
+// re-quantized in the same kernel.  One 128-thread CTA per (sequence, kv
+// head, K|V) tile reads the 15 other rows from the fp16 pool, takes the new
+// row from the input (and writes it to the fp16 pool), then quantizes the
+// tile exactly as the quantize kernel does: bit-identical codes and scale to
+// quantizing the tile after a plain fp16 append.  Latency-bound for a decode
+// batch: 4 KiB read and about 2.3 KiB written per tile at head_dim 128.
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -82,10 +82,10 @@ __global__ void __launch_bounds__(kAppendThreads)
     }
 }
 
-template <int kHeadDim>
+template <int kHeadDim, bool kFp8>
 __global__ void __launch_bounds__(kQuantThreads)
     append_int8_kernel(__half *__restrict__ k_pool, __half *__restrict__ v_pool,
-                       int8_t *__restrict__ k_codes, int8_t *__restrict__ v_codes,
+                       uint8_t *__restrict__ k_codes, uint8_t *__restrict__ v_codes,
                        float *__restrict__ k_scales, float *__restrict__ v_scales,
                        const __half *__restrict__ k_new, const __half *__restrict__ v_new,
                        const int32_t *__restrict__ block_tables, int max_blocks_per_seq,
@@ -126,13 +126,14 @@ __global__ void __launch_bounds__(kQuantThreads)
             }
         }
         const float amax = cta_absmax(chunks_absmax(raw), warp_max);
-        const float scale = __fdiv_rn(amax, 127.0f);
+        const float scale = __fdiv_rn(amax, kFp8 ? 448.0f : 127.0f);
         const float rcp = __frcp_rn(scale);
         uint2 *dst =
             reinterpret_cast<uint2 *>(is_v ? v_codes : k_codes) + tile * kTileChunks;
 #pragma unroll
         for (int c = 0; c < kChunks; ++c)
-            dst[c * kQuantThreads + threadIdx.x] = chunk_codes(raw[c], scale, rcp);
+            dst[c * kQuantThreads + threadIdx.x] =
+                kFp8 ? chunk_codes_fp8(raw[c], scale) : chunk_codes(raw[c], scale, rcp);
         if (threadIdx.x == 0) (is_v ? v_scales : k_scales)[tile] = scale;
     }
 }
@@ -206,15 +207,15 @@ extern "C" pkv_status pkv_append_fp16(void *k_cache, void *v_cache, int num_bloc
                       row_chunks, num_blocks, dev_status);
 }
 
-extern "C" pkv_status pkv_append_int8(void *k_cache, void *v_cache, int8_t *k_codes,
-                                      int8_t *v_codes, float *k_scales, float *v_scales,
-                                      int num_blocks, const void *k_new, const void *v_new,
-                                      const int32_t *block_tables, int max_blocks_per_seq,
-                                      const int32_t *positions, int num_seqs, int num_kv_heads,
-                                      int head_dim, int block_size, int32_t *dev_status,
-                                      void *stream)
+namespace pkv {
+namespace {
+
+pkv_status append_codes(void *k_cache, void *v_cache, void *k_codes, void *v_codes,
+                        float *k_scales, float *v_scales, int num_blocks, const void *k_new,
+                        const void *v_new, const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *positions, int num_seqs, int num_kv_heads, int head_dim,
+                        int block_size, int32_t *dev_status, void *stream, bool fp8)
 {
-    using namespace pkv;
     const pkv_status st =
         check_append(k_cache, v_cache, k_new, v_new, num_blocks, block_tables,
                      max_blocks_per_seq, positions, num_seqs, num_kv_heads, head_dim,
@@ -232,13 +233,53 @@ extern "C" pkv_status pkv_append_int8(void *k_cache, void *v_cache, int8_t *k_co
     if (grid > cap) grid = cap;
     __half *kp = static_cast<__half *>(k_cache), *vp = static_cast<__half *>(v_cache);
     const __half *kn = static_cast<const __half *>(k_new), *vn = static_cast<const __half *>(v_new);
-    return head_dim == 128
-               ? launch_pdl(append_int8_kernel<128>, grid, kQuantThreads, stream, kp, vp,
-                            k_codes, v_codes, k_scales, v_scales, kn, vn, block_tables,
+    uint8_t *kc = static_cast<uint8_t *>(k_codes), *vc = static_cast<uint8_t *>(v_codes);
+    if (head_dim == 128)
+        return fp8 ? launch_pdl(append_int8_kernel<128, true>, grid, kQuantThreads, stream, kp,
+                                vp, kc, vc, k_scales, v_scales, kn, vn, block_tables,
+                                max_blocks_per_seq, positions, num_seqs, num_kv_heads,
+                                num_blocks, dev_status)
+                   : launch_pdl(append_int8_kernel<128, false>, grid, kQuantThreads, stream, kp,
+                                vp, kc, vc, k_scales, v_scales, kn, vn, block_tables,
+                                max_blocks_per_seq, positions, num_seqs, num_kv_heads,
+                                num_blocks, dev_status);
+    return fp8 ? launch_pdl(append_int8_kernel<64, true>, grid, kQuantThreads, stream, kp, vp,
+                            kc, vc, k_scales, v_scales, kn, vn, block_tables,
                             max_blocks_per_seq, positions, num_seqs, num_kv_heads, num_blocks,
                             dev_status)
-               : launch_pdl(append_int8_kernel<64>, grid, kQuantThreads, stream, kp, vp,
-                            k_codes, v_codes, k_scales, v_scales, kn, vn, block_tables,
+               : launch_pdl(append_int8_kernel<64, false>, grid, kQuantThreads, stream, kp, vp,
+                            kc, vc, k_scales, v_scales, kn, vn, block_tables,
                             max_blocks_per_seq, positions, num_seqs, num_kv_heads, num_blocks,
                             dev_status);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_append_int8(void *k_cache, void *v_cache, int8_t *k_codes,
+                                      int8_t *v_codes, float *k_scales, float *v_scales,
+                                      int num_blocks, const void *k_new, const void *v_new,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *positions, int num_seqs, int num_kv_heads,
+                                      int head_dim, int block_size, int32_t *dev_status,
+                                      void *stream)
+{
+    return pkv::append_codes(k_cache, v_cache, k_codes, v_codes, k_scales, v_scales, num_blocks,
+                             k_new, v_new, block_tables, max_blocks_per_seq, positions,
+                             num_seqs, num_kv_heads, head_dim, block_size, dev_status, stream,
+                             false);
+}
+
+extern "C" pkv_status pkv_append_fp8(void *k_cache, void *v_cache, uint8_t *k_codes,
+                                     uint8_t *v_codes, float *k_scales, float *v_scales,
+                                     int num_blocks, const void *k_new, const void *v_new,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *positions, int num_seqs, int num_kv_heads,
+                                     int head_dim, int block_size, int32_t *dev_status,
+                                     void *stream)
+{
+    return pkv::append_codes(k_cache, v_cache, k_codes, v_codes, k_scales, v_scales, num_blocks,
+                             k_new, v_new, block_tables, max_blocks_per_seq, positions,
+                             num_seqs, num_kv_heads, head_dim, block_size, dev_status, stream,
+                             true);
 }

@@ -14,7 +14,7 @@ from gpu_common import assert_close, dev, ensure_built, oracle_codes
 pytestmark = pytest.mark.gpu
 
 
-def gpu_append(kp, vp, kn, vn, tables, pos, codes=None):
+def gpu_append(kp, vp, kn, vn, tables, pos, codes=None, fp8=False):
     """Run one append on device copies; returns device tensors and the status."""
     ensure_built()
     kd, vd = dev(kp), dev(vp)
@@ -25,7 +25,8 @@ def gpu_append(kp, vp, kn, vn, tables, pos, codes=None):
         dc = None
     else:
         dc = tuple(dev(c) for c in codes)
-        pkv.pkv_append_int8(kd, vd, *dc, *args, dev_status=status)
+        fn = pkv.pkv_append_fp8 if fp8 else pkv.pkv_append_int8
+        fn(kd, vd, *dc, *args, dev_status=status)
     torch.cuda.synchronize()
     return kd, vd, dc, int(status.item())
 
@@ -50,13 +51,16 @@ def test_append_fp16_and_int8_bit_exact(hq, hkv, d):
     kd, vd, _, st = gpu_append(w.k_pool, w.v_pool, kn, vn, w.block_tables, pos)
     assert st == 0 and same_bits(kd, rk) and same_bits(vd, rv)
 
-    codes = oracle_codes(w)
-    ref = oracle.append_int8(w.k_pool, w.v_pool, *codes, kn, vn, w.block_tables, pos)
-    kd, vd, dc, st = gpu_append(w.k_pool, w.v_pool, kn, vn, w.block_tables, pos, codes)
-    assert st == 0
-    assert same_bits(kd, ref[0]) and same_bits(vd, ref[1])
-    for got, want in zip(dc, (ref[2], ref[3], ref[4], ref[5])):
-        assert same_bits(got, want)
+    for fp8 in (False, True):
+        codes = oracle_codes(w, fp8)
+        app = oracle.append_fp8 if fp8 else oracle.append_int8
+        ref = app(w.k_pool, w.v_pool, *codes, kn, vn, w.block_tables, pos)
+        kd, vd, dc, st = gpu_append(w.k_pool, w.v_pool, kn, vn, w.block_tables, pos, codes,
+                                    fp8=fp8)
+        assert st == 0
+        assert same_bits(kd, ref[0]) and same_bits(vd, ref[1])
+        for got, want in zip(dc, (ref[2], ref[3], ref[4], ref[5])):
+            assert same_bits(got, want)
 
 
 @pytest.mark.parametrize("d", [64, 128])
