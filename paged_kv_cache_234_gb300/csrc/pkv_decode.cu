@@ -12,9 +12,9 @@
 // Work decomposition.  A work item is (sequence, kv head, group of up to 8
 // query heads of that kv head); its pages are the sequence's 16-token
 // blocks.  All items' pages form one stream of T pages, and every warp of a
-// persistent grid (one worker per resident warp) streams one contiguous,
-// equal share of it, so every SM moves the same number of bytes whatever the
-// mix of context lengths.  A worker's share is a run of "pieces": at most one
+// persistent grid (one worker per resident warp, at most four per item)
+// streams one contiguous, equal share of it, so every SM moves the same
+// number of bytes whatever the mix of context lengths.  A worker's share is a run of "pieces": at most one
 // partial item at each end and whole items in between.  Whole items are
 // finished in place; a partial piece leaves (running max, running sum,
 // unnormalised accumulator) in the workspace, and the split-context reduce
