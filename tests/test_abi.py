@@ -100,6 +100,58 @@ def test_decode_host_validation(L, int8):
         assert _decode(L, int8, vs=FAKE + 2) == pkv.PKV_ERR_MISALIGNED
 
 
+def test_fp8_entry_points_host_validation(L):
+    # decode: same argument rules as INT8
+    a = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, FAKE, 4, FAKE, 64, 2, 8, 2, 64, 16, 0.125,
+         FAKE, 1 << 30, None, None]
+    def dec(i=None, v=None):
+        b = list(a)
+        if i is not None:
+            b[i] = v
+        return L.pkv_paged_decode_fp8(*b)
+    assert dec(0, None) == pkv.PKV_ERR_INVALID_ARG          # out
+    assert dec(4, None) == pkv.PKV_ERR_INVALID_ARG          # k_scales
+    assert dec(14, 96) == pkv.PKV_ERR_UNSUPPORTED           # head_dim
+    assert dec(2, FAKE + 4) == pkv.PKV_ERR_MISALIGNED       # k_codes
+    assert dec(18, 100) == pkv.PKV_ERR_WORKSPACE
+    assert dec(11, 0) == pkv.PKV_OK                         # no sequences, nothing launched
+    # quantize
+    q = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 16, 2, 64, 16, None, None]
+    def qz(i=None, v=None):
+        b = list(q)
+        if i is not None:
+            b[i] = v
+        return L.pkv_quantize_blocks_fp8(*b)
+    assert qz(2, None) == pkv.PKV_ERR_INVALID_ARG
+    assert qz(10, 96) == pkv.PKV_ERR_UNSUPPORTED
+    assert qz(3, FAKE + 1) == pkv.PKV_ERR_MISALIGNED
+    assert qz(6, FAKE) == pkv.PKV_OK                        # empty id list
+    # append
+    ap = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, FAKE, FAKE, FAKE, 4, FAKE, 2, 2, 64, 16, None,
+          None]
+    def app(i=None, v=None):
+        b = list(ap)
+        if i is not None:
+            b[i] = v
+        return L.pkv_append_fp8(*b)
+    assert app(4, None) == pkv.PKV_ERR_INVALID_ARG
+    assert app(3, FAKE + 8) == pkv.PKV_ERR_MISALIGNED
+    assert app(12, 0) == pkv.PKV_OK
+
+
+def test_block_manager_null_handle_and_arguments(L):
+    assert L.pkv_bm_create(4, 16, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_bm_allocate(None, None, 1, FAKE) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_bm_free(None, FAKE, 1) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_bm_stats(None, None) == pkv.PKV_ERR_INVALID_ARG
+    bm = pkv.BlockManager(4)
+    assert L.pkv_bm_allocate(bm._h, None, -1, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_bm_allocate(bm._h, None, 2, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_bm_refcounts(bm._h, None, 4) == pkv.PKV_ERR_INVALID_ARG
+    bm.close()
+    L.pkv_bm_destroy(None)  # a no-op
+
+
 def test_quantize_host_validation(L):
     def q(**kw):
         a = dict(k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE, ids=None, nids=0,
