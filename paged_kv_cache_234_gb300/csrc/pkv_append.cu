@@ -9,8 +9,8 @@
 // fp16 values is 8 or 16 threads, so a warp writes 2 or 4 full rows.
 //
 // INT8 (or FP8 E4M3) cache: the written (block, kv head) tile is
-// re-quantized in the same kernel.  One 128-thread CTA per (sequence, kv
-// head, K|V) tile reads the 15 other rows from the fp16 pool, takes the new
+// re-quantized in the same kernel.  One CTA per (sequence, kv head, K|V)
+// tile (a thread per 16-byte chunk) reads the 15 other rows from the fp16 pool, takes the new
 // row from the input (and writes it to the fp16 pool), then quantizes the
 // tile exactly as the quantize kernel does: bit-identical codes and scale to
 // quantizing the tile after a plain fp16 append.  Latency-bound for a decode
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kAppendThreads)
 }
 
 template <int kHeadDim, bool kFp8>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(tile_threads<kHeadDim>())
     append_int8_kernel(__half *__restrict__ k_pool, __half *__restrict__ v_pool,
                        uint8_t *__restrict__ k_codes, uint8_t *__restrict__ v_codes,
                        float *__restrict__ k_scales, float *__restrict__ v_scales,
@@ -94,8 +94,9 @@ __global__ void __launch_bounds__(kQuantThreads)
 {
     constexpr int kRowChunks = kHeadDim / 8;                  // 16-byte chunks per row
     constexpr int kTileChunks = 16 * kRowChunks;
-    constexpr int kChunks = kTileChunks / kQuantThreads;      // per thread
-    __shared__ float warp_max[kQuantThreads / 32];
+    constexpr int kThreads = tile_threads<kHeadDim>();       // one chunk per thread
+    constexpr int kChunks = kTileChunks / kThreads;
+    __shared__ float warp_max[kThreads / 32];
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     const int64_t tiles = static_cast<int64_t>(num_seqs) * num_kv_heads;
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kQuantThreads)
         uint4 raw[kChunks];
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
-            const int idx = c * kQuantThreads + threadIdx.x;
+            const int idx = c * kThreads + threadIdx.x;
             if (idx / kRowChunks == slot) {
                 raw[c] = __ldg(fresh + (idx % kRowChunks));
                 pool[idx] = raw[c];
@@ -125,14 +126,14 @@ __global__ void __launch_bounds__(kQuantThreads)
                 raw[c] = pool[idx];
             }
         }
-        const float amax = cta_absmax(chunks_absmax(raw), warp_max);
+        const float amax = cta_absmax<kThreads>(chunks_absmax(raw), warp_max);
         const float scale = __fdiv_rn(amax, kFp8 ? 448.0f : 127.0f);
         const float rcp = __frcp_rn(scale);
         uint2 *dst =
             reinterpret_cast<uint2 *>(is_v ? v_codes : k_codes) + tile * kTileChunks;
 #pragma unroll
         for (int c = 0; c < kChunks; ++c)
-            dst[c * kQuantThreads + threadIdx.x] =
+            dst[c * kThreads + threadIdx.x] =
                 kFp8 ? chunk_codes_fp8(raw[c], scale) : chunk_codes(raw[c], scale, rcp);
         if (threadIdx.x == 0) (is_v ? v_scales : k_scales)[tile] = scale;
     }
@@ -235,19 +236,19 @@ pkv_status append_codes(void *k_cache, void *v_cache, void *k_codes, void *v_cod
     const __half *kn = static_cast<const __half *>(k_new), *vn = static_cast<const __half *>(v_new);
     uint8_t *kc = static_cast<uint8_t *>(k_codes), *vc = static_cast<uint8_t *>(v_codes);
     if (head_dim == 128)
-        return fp8 ? launch_pdl(append_int8_kernel<128, true>, grid, kQuantThreads, stream, kp,
+        return fp8 ? launch_pdl(append_int8_kernel<128, true>, grid, tile_threads<128>(), stream, kp,
                                 vp, kc, vc, k_scales, v_scales, kn, vn, block_tables,
                                 max_blocks_per_seq, positions, num_seqs, num_kv_heads,
                                 num_blocks, dev_status)
-                   : launch_pdl(append_int8_kernel<128, false>, grid, kQuantThreads, stream, kp,
+                   : launch_pdl(append_int8_kernel<128, false>, grid, tile_threads<128>(), stream, kp,
                                 vp, kc, vc, k_scales, v_scales, kn, vn, block_tables,
                                 max_blocks_per_seq, positions, num_seqs, num_kv_heads,
                                 num_blocks, dev_status);
-    return fp8 ? launch_pdl(append_int8_kernel<64, true>, grid, kQuantThreads, stream, kp, vp,
+    return fp8 ? launch_pdl(append_int8_kernel<64, true>, grid, tile_threads<64>(), stream, kp, vp,
                             kc, vc, k_scales, v_scales, kn, vn, block_tables,
                             max_blocks_per_seq, positions, num_seqs, num_kv_heads, num_blocks,
                             dev_status)
-               : launch_pdl(append_int8_kernel<64, false>, grid, kQuantThreads, stream, kp, vp,
+               : launch_pdl(append_int8_kernel<64, false>, grid, tile_threads<64>(), stream, kp, vp,
                             kc, vc, k_scales, v_scales, kn, vn, block_tables,
                             max_blocks_per_seq, positions, num_seqs, num_kv_heads, num_blocks,
                             dev_status);

@@ -61,8 +61,9 @@ __device__ __forceinline__ float chunks_absmax(const uint4 (&raw)[kChunks])
     return amax;
 }
 
-// CTA-wide max of the per-thread values; warp_max holds kQuantThreads / 32
-// floats of shared memory and may be reused once this returns.
+// CTA-wide max of the per-thread values over kThreads threads; warp_max holds
+// kThreads / 32 floats of shared memory and may be reused once this returns.
+template <int kThreads = kQuantThreads>
 __device__ __forceinline__ float cta_absmax(float amax, float *warp_max)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -71,9 +72,16 @@ __device__ __forceinline__ float cta_absmax(float amax, float *warp_max)
     if (lane == 0) warp_max[warp] = amax;
     __syncthreads();
 #pragma unroll
-    for (int w = 0; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+    for (int w = 0; w < kThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
     __syncthreads();
     return amax;
+}
+
+// Threads of a one-tile CTA: one 16-byte chunk (8 values) each.
+template <int kHeadDim>
+__host__ __device__ constexpr int tile_threads()
+{
+    return 16 * kHeadDim / 8;
 }
 
 // Eight codes of one 16-byte chunk, packed little-endian into a uint2.

@@ -4,14 +4,15 @@
 // same with FP8 (OCP E4M3) codes and scale = amax / 448 ("PagedAttention &
 // KV-Cache Memory Management", section 5.1: per-block scaled FP8 KV).
 //
-// One 128-thread CTA per (block, kv head, K|V) tile of 16 x head_dim fp16
-// values (grid-strided when there are many tiles).  The tile is read once with
+// One CTA per (block, kv head, K|V) tile of 16 x head_dim fp16 values, one
+// thread per 16-byte chunk (256 threads at head_dim 128; grid-strided when
+// there are many tiles).  The tile is read once with
 // 16-byte loads (coalesced), max |x| is reduced with warp shuffles and shared
 // memory, scale = max / 127 with an IEEE fp32 division, and every code is the
 // half-even rounding of the IEEE fp32 quotient x / scale.  HBM-bound for large
 // jobs: 2 bytes read and 1 byte written per value, plus 4 bytes of scale per
-// tile; for a decode step's few tail blocks it is latency-bound, hence the
-// many threads per tile.
+// tile; for a decode step's few tail blocks it is latency-bound, hence one
+// chunk per thread.
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -23,7 +24,7 @@ namespace pkv {
 namespace {
 
 template <int kHeadDim, bool kFp8>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(tile_threads<kHeadDim>())
     quantize_kernel(const __half *__restrict__ k_in, const __half *__restrict__ v_in,
                     uint8_t *__restrict__ k_out, uint8_t *__restrict__ v_out,
                     float *__restrict__ k_scales, float *__restrict__ v_scales,
@@ -31,8 +32,9 @@ __global__ void __launch_bounds__(kQuantThreads)
                     int num_kv_heads, int num_blocks, int32_t *dev_status)
 {
     constexpr int kTileElems = 16 * kHeadDim;
-    constexpr int kChunks = kTileElems / 8 / kQuantThreads;  // 16-byte chunks per thread
-    __shared__ float warp_max[kQuantThreads / 32];
+    constexpr int kThreads = tile_threads<kHeadDim>();
+    constexpr int kChunks = kTileElems / 8 / kThreads;  // 16-byte chunks per thread (1)
+    __shared__ float warp_max[kThreads / 32];
     // programmatic dependent launch: the previous kernel's writes (and its
     // reads of the pools this kernel overwrites) are complete past this point
     ptx::griddep_wait();
@@ -55,15 +57,15 @@ __global__ void __launch_bounds__(kQuantThreads)
 
         uint4 raw[kChunks];
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) raw[c] = __ldcs(src + c * kQuantThreads + threadIdx.x);
+        for (int c = 0; c < kChunks; ++c) raw[c] = __ldcs(src + c * kThreads + threadIdx.x);
 
-        const float amax = cta_absmax(chunks_absmax(raw), warp_max);
+        const float amax = cta_absmax<kThreads>(chunks_absmax(raw), warp_max);
         const float scale = __fdiv_rn(amax, kFp8 ? 448.0f : 127.0f);
         const float rcp = __frcp_rn(scale);
 
 #pragma unroll
         for (int c = 0; c < kChunks; ++c)
-            __stcs(dst + c * kQuantThreads + threadIdx.x,
+            __stcs(dst + c * kThreads + threadIdx.x,
                    kFp8 ? chunk_codes_fp8(raw[c], scale) : chunk_codes(raw[c], scale, rcp));
         if (threadIdx.x == 0) (is_v ? v_scales : k_scales)[tile] = scale;
     }
@@ -99,7 +101,7 @@ pkv_status quantize_entry(const void *k_fp16, const void *v_fp16, void *k_codes,
     const int64_t cap = static_cast<int64_t>(di.num_sms) * 16;
     if (grid > cap) grid = cap;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const dim3 g(static_cast<unsigned>(grid)), b(kQuantThreads);
+    const dim3 g(static_cast<unsigned>(grid)), b(16 * head_dim / 8);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = g;
     cfg.blockDim = b;
