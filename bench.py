@@ -361,9 +361,10 @@ def run_profile_small(args):
 
 def run_report(args):
     """Per configuration and variant: p50 / p90 us per decode call over 200
-    timed calls after 20 warm-ups, L2 flushed before each call; KV GB/s of
-    the logical bytes (unique bytes too where sequences share blocks) and
-    sequence-steps/s.  One JSON line per (configuration, variant)."""
+    timed calls after 20 warm-ups (--report-calls, --report-warmup), L2
+    flushed before each call; KV GB/s of the logical bytes (unique bytes too
+    where sequences share blocks) and sequence-steps/s.  One JSON line per
+    (configuration, variant), in the order the calls run."""
     import torch
     import paged_kv_cache_234_gb300 as pkv
     from paged_kv_cache_234_gb300 import build as pkv_build
@@ -402,10 +403,10 @@ def run_report(args):
         # blocks read once per call when sequences share them (c4: shared prefix)
         uniq_ctx = np.full(w.used_block_ids.size, 16, np.int64)
         for variant, fn in calls.items():
-            for _ in range(20):
+            for _ in range(args.report_warmup):
                 fn()
             ts = []
-            for _ in range(200):
+            for _ in range(args.report_calls):
                 fw.zero_()
                 fr.view(torch.int32).max()
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -451,6 +452,8 @@ def main():
     ap.add_argument("--report-configs", action="store_true",
                     help="p50/p90 of every decode variant on every configuration, one JSON "
                          "line each (no benchmark line)")
+    ap.add_argument("--report-warmup", type=int, default=20)
+    ap.add_argument("--report-calls", type=int, default=200)
     ap.add_argument("--profile", choices=["int8", "fp8", "fp16", "quantize", "append", "evict"],
                     help="profiling run: the same batch over a 16384-block pool (eviction: "
                          "a 65536-block pool), only warm-up + timed calls of one kernel, "
