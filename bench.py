@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -140,7 +141,9 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # the raw samples: PKV_CLOCKS_DIR if set, else the system temp folder
+        folder = os.environ.get("PKV_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(folder, f"pkv_clocks_rank{index}.csv")
 
     def start(self):
         try:
