@@ -1,9 +1,10 @@
 /*
  * pkv.h -- C ABI of libpkv: decode-step paged attention over a
- * block-table-indexed KV cache, fp16 or INT8 KV, for NVIDIA GB300 (sm_103a),
- * with the per-(block, kv head) INT8 quantizer, the token append that
- * precedes a decode step, and eviction scoring with the choice of the blocks
- * to evict.
+ * block-table-indexed KV cache, fp16, INT8 or FP8 (E4M3) KV, for NVIDIA GB300
+ * (sm_103a), with the per-(block, kv head) INT8 and FP8 quantizers, the token
+ * append that precedes a decode step, eviction scoring with the choice of the
+ * blocks to evict, and a host block manager (free list, reference counts,
+ * prefix sharing, copy-on-write) whose page copies run on the GPU.
  *
  * Sources for what each call computes:
  *  [PKF]  "PagedKV-Fusion" README (INT8 per-(block, head) quantized decode
@@ -30,7 +31,8 @@
  *   context_lens   [num_seqs]                        int32
  *   out            [num_seqs][num_heads][head_dim]  fp32
  * Query head h attends with kv head h / (num_heads / num_kv_heads).
- * Supported: block_size 16; head_dim 64 or 128; any group size.
+ * Supported: block_size 16; head_dim 64 or 128; any group size; decode
+ * batches of up to 8192 sequences (PKV_ERR_UNSUPPORTED beyond).
  *
  * Errors.  Host-side argument errors are returned before anything is
  * launched.  Device-side data errors never trap: the affected outputs are
@@ -412,7 +414,7 @@ PKV_API pkv_status pkv_copy_blocks(void *const *pools, const int64_t *block_byte
                                    int num_pairs, int32_t *dev_status, void *stream);
 
 /*
- * Bytes of workspace a decode call with these sizes needs (either variant).
+ * Bytes of workspace a decode call with these sizes needs (any KV variant).
  * Pure host arithmetic: no CUDA call.  Returns 0 for invalid sizes.
  */
 PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
