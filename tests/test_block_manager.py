@@ -136,3 +136,47 @@ def test_create_rejects_bad_sizes():
     bm = pkv.BlockManager(0)
     assert refused(bm.allocate, 1) == pkv.PKV_ERR_EXHAUSTED
     assert bm.allocate(0).size == 0
+
+
+def test_threads_share_one_manager():
+    # every call takes the manager's lock: eight threads allocating (some
+    # blocks shared by prefix hash across threads), forking, copying on write
+    # and freeing leave the manager consistent and, at the end, fully free
+    import threading
+
+    bm = pkv.BlockManager(4096)
+    errors = []
+
+    def worker(tid):
+        rng = random.Random(1000 + tid)
+        try:
+            for _ in range(300):
+                held = []
+                n = rng.randint(1, 16)
+                hashes = [rng.choice([NO_HASH, NO_HASH, 7 + rng.randrange(8)]) for _ in range(n)]
+                ids = bm.allocate(hashes)
+                fresh = [int(b) for b, h in zip(ids, hashes) if h == NO_HASH]
+                assert len(set(fresh)) == len(fresh)
+                held += [int(b) for b in ids]
+                if rng.random() < 0.5:
+                    f = [int(b) for b in ids[: rng.randint(1, n)]]
+                    bm.fork(f)
+                    held += f
+                if rng.random() < 0.5:
+                    k = rng.randint(1, len(held))
+                    src = held[:k]
+                    new, _ = bm.cow(src)
+                    held = [int(b) for b in new] + held[k:]
+                bm.free(held)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:3]
+    st = bm.stats()
+    assert st["free"] == 4096 and st["used"] == 0 and st["logical"] == 0
+    assert not bm.refcounts().any()
