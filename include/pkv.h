@@ -424,8 +424,8 @@ PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv
  * Tuning and test control: cap the number of decode workers (one worker =
  * one warp streaming a contiguous range of KV pages; each range ends in a
  * partial result that the split-context reduce merges).  0 restores the
- * automatic choice (every resident warp of the device, at most four per
- * item).  Process-wide.
+ * automatic choice (every resident warp of the device -- about seven per SM
+ * for fp16 KV at head_dim 128 -- and at most four per item).  Process-wide.
  */
 PKV_API pkv_status pkv_set_decode_workers(int max_workers);
 

@@ -12,7 +12,8 @@
 // Work decomposition.  A work item is (sequence, kv head, group of up to 8
 // query heads of that kv head); its pages are the sequence's 16-token
 // blocks.  All items' pages form one stream of T pages, and every warp of a
-// persistent grid (one worker per resident warp, at most four per item)
+// persistent grid (one worker per resident warp -- about seven per SM for
+// fp16 at head_dim 128 -- and at most four per item)
 // streams one contiguous, equal share of it, so every SM moves the same
 // number of bytes whatever the mix of context lengths.  A worker's share is a run of "pieces": at most one
 // partial item at each end and whole items in between.  Whole items are
@@ -109,6 +110,13 @@ struct DecodeArgs {
 #ifndef PKV_I8_D128_CTAS
 #define PKV_I8_D128_CTAS 3
 #endif
+// fp16 d128: workers per SM (0: every resident warp).  Measured on GB300: the
+// fp16 kernel moves its pages faster with ~7 streaming warps per SM than with
+// all 12 (64 x 2048: 93.6 against 101.4 us per call; 256 ragged sequences:
+// 322.7 against 339.8 us), while the INT8 and FP8 kernels need every warp.
+#ifndef PKV_F16_D128_WARPS_PER_SM
+#define PKV_F16_D128_WARPS_PER_SM 7
+#endif
 
 template <int kPPS_, int kStages_, int kMinCtas_>
 struct Tune {
@@ -151,6 +159,7 @@ struct Cfg {
     static constexpr int kSwizzle = kRowBytes >= 128 ? 128 : 64;
     static constexpr int kStages = TuneOf<kKv, kD>::kStages;
     static constexpr int kMinCtas = TuneOf<kKv, kD>::kMinCtas;
+    static constexpr int kWarpsPerSm = kKv == kKvF16 && kD == 128 ? PKV_F16_D128_WARPS_PER_SM : 0;
     static_assert(kPPS == 1 || kPPS == 2, "one or two pages per stage");
     static constexpr int kHdrBytes = 32;  // per stage: bad[2], k scale[2], v scale[2]
     static constexpr int kStageRegion = kWarps * kStages * kStageBytes;
@@ -859,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
 // range holds the first piece of a split item merges that item:
 //   out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w,  M = max_w m_w
 // over the pieces of workers first .. last.  A piece flagged bad (l < 0)
-// zeroes the item.  With up to four pieces (the usual case) every load of
+// zeroes the item.  With up to eight pieces (the usual case) every load of
 // every piece is issued at once; otherwise lanes read the (m, l) of up to 32
 // pieces at a time, then the accumulators four pieces per batch.  Lanes run
 // across head_dim; pieces are combined in a fixed order.
@@ -898,20 +907,30 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const DecodeArgs p)
     for (int i = 0; i < kD / 32; ++i) acc[i] = 0.f;
     float L = 0.f;
     bool bad = false;
-    if (nw <= 4) {
+    constexpr int kFast = 8;  // pieces whose loads are all issued at once
+    if (nw <= kFast) {
         // common case: every load of every piece issued at once
-        float m[4], l[4], v[4][kD / 32];
+        float m[kFast], l[kFast], v[kFast][kD / 32];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kFast; ++j) {
             const float *r = j < nw ? rec_of(j) : nullptr;
-            m[j] = r ? __ldcg(r) : -INFINITY;
-            l[j] = r ? __ldcg(r + 1) : 0.f;
+            if (r) {
+                m[j] = __ldcg(r);
+                l[j] = __ldcg(r + 1);
 #pragma unroll
-            for (int i = 0; i < kD / 32; ++i) v[j][i] = r ? __ldcg(r + 4 + lane + 32 * i) : 0.f;
+                for (int i = 0; i < kD / 32; ++i) v[j][i] = __ldcg(r + 4 + lane + 32 * i);
+            } else {
+                m[j] = -INFINITY;
+                l[j] = 0.f;
+#pragma unroll
+                for (int i = 0; i < kD / 32; ++i) v[j][i] = 0.f;
+            }
         }
-        const float M = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+        float M = m[0];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 1; j < kFast; ++j) M = fmaxf(M, m[j]);
+#pragma unroll
+        for (int j = 0; j < kFast; ++j) {
             const float f = m[j] == -INFINITY ? 0.f : ptx::ex2(m[j] - M);
             bad |= l[j] < 0.f;
             L += f * l[j];
@@ -1090,6 +1109,8 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     }
     if (per_sm <= 0) return PKV_ERR_UNSUPPORTED;
     int64_t workers = static_cast<int64_t>(per_sm) * di.num_sms * kWarps;
+    if (C::kWarpsPerSm > 0 && workers > static_cast<int64_t>(C::kWarpsPerSm) * di.num_sms)
+        workers = static_cast<int64_t>(C::kWarpsPerSm) * di.num_sms;
     if (workers > kMaxWorkers) workers = kMaxWorkers;
     if (cap > 0 && workers > cap) workers = cap;
     if (workers > sh.max_pages) workers = sh.max_pages;
