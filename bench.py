@@ -208,6 +208,14 @@ def _subpool(w, seqs):
             lens, tails)
 
 
+def workload_desc(w, n_tails):
+    """The benchmark workload as named in both arms' "config"."""
+    n, hq, d = w.query.shape
+    return (f"{CONFIG}: {n} seqs x ctx {w.max_context_len}, {hq} q / {w.num_kv_heads} kv heads, "
+            f"head_dim {d}, block 16, pool {w.num_blocks} blocks; step = INT8 quantize of "
+            f"{n_tails} tail blocks + INT8 decode")
+
+
 def run_reference(args, ws, rank):
     """CPU oracle on a bounded sample of the workload (rank 0 only): each step
     quantizes the tail blocks of 8 of the 64 sequences and decodes those 8."""
@@ -239,8 +247,8 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t_total / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{CONFIG} (CPU oracle on {sample} of {w.num_seqs} sequences "
-                               "per step)"},
+        "config": {"workload": workload_desc(w, len(w.tail_block_ids())),
+                   "sample": f"CPU oracle on {sample} of {w.num_seqs} sequences per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{sample} of {w.num_seqs} sequences per step: INT8 "
                                    "quantize of their tail blocks + fp64 INT8 decode"},
@@ -693,9 +701,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8-kv f16-mma f32-acc",
         "data": "synthetic",
-        "config": {"workload": f"{CONFIG}: {n} seqs x ctx {mcl}, {hq} q / {hkv} kv heads, "
-                               f"head_dim {d}, block 16, pool {w.num_blocks} blocks; step = "
-                               f"INT8 quantize of {len(tails_np)} tail blocks + INT8 decode",
+        "config": {"workload": workload_desc(w, len(tails_np)),
                    "l2": "flushed between steps, outside the events: 256 MiB written, then "
                          "256 MiB read (L2 left clean); inputs are also larger than L2",
                    "parallelism": f"weak: the batch replicated per GPU x{ws}"},
