@@ -413,6 +413,7 @@ def run_report(args):
         }
         # blocks read once per call when sequences share them (c4: shared prefix)
         uniq_ctx = np.full(w.used_block_ids.size, 16, np.int64)
+        cpu = None if args.no_cpu_baseline else cpu_oracle_sample(w, W.CONFIG_NAMES.index(name))
         for variant, fn in calls.items():
             for _ in range(args.report_warmup):
                 fn()
@@ -431,12 +432,41 @@ def run_report(args):
             b = decode_bytes(w.context_lens, hkv, d, eb, sc)
             bu = decode_bytes(uniq_ctx, hkv, d, eb, sc)
             t50, t90 = statistics.median(ts), float(np.percentile(ts, 90))
-            print(json.dumps({"config": name, "variant": variant, "p50_us": 1e6 * t50,
-                              "p90_us": 1e6 * t90, "kv_bytes": b, "unique_kv_bytes": bu,
-                              "GB/s": b / t50 / 1e9, "frac_of_peak": b / t50 / 1e9 / peak,
-                              "seq_steps_per_s": n / t50}), flush=True)
+            rec = {"config": name, "variant": variant, "p50_us": 1e6 * t50,
+                   "p90_us": 1e6 * t90, "kv_bytes": b, "unique_kv_bytes": bu,
+                   "GB/s": b / t50 / 1e9, "frac_of_peak": b / t50 / 1e9 / peak,
+                   "seq_steps_per_s": n / t50}
+            if variant == "int8" and cpu is not None:
+                rec["cpu_oracle"] = {**cpu, "us_scaled": 1e6 * b / (cpu["GB/s"] * 1e9)}
+            print(json.dumps(rec), flush=True)
         del kf, vf, pools
         torch.cuda.empty_cache()
+
+
+def cpu_oracle_sample(w, seed, sample=8, seconds=0.5):
+    """The oracle's INT8 decode on a seeded sample of at most `sample` of the
+    batch's sequences, on this host's cores: its KV GB/s (the per-configuration
+    CPU baseline; the whole batch's time is its bytes at this rate)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    k = min(sample, w.num_seqs)
+    seqs = np.sort(rng.choice(w.num_seqs, size=k, replace=False))
+    kp, vp, tab, lens, _ = _subpool(w, seqs)
+    kc, ks = oracle.quantize(kp)
+    vc, vs = oracle.quantize(vp)
+    nb = decode_bytes(lens, w.num_kv_heads, w.head_dim, 1, True)
+    threads = oracle.max_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_int8(w.query[seqs], kc, vc, ks, vs, tab, lens,
+                           num_kv_heads=w.num_kv_heads, softmax_scale=w.softmax_scale,
+                           num_threads=threads)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"GB/s": nb * reps / dt / 1e9, "threads": threads,
+            "sample": f"{k} of {w.num_seqs} sequences (seeded), {reps} repetitions"}
 
 
 def evict_cpu_us(num_blocks, reps=20):
