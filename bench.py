@@ -628,6 +628,16 @@ def main():
     f8_ms = timed(decode_fp8, Kd)
     q_ms = timed(step_int8, Kd)
 
+    # labelled extra: the same step (tail quantize + INT8 decode) captured once
+    # in a CUDA graph and replayed, L2 still flushed outside each replay
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step_int8()
+        decode_int8()
+    for _ in range(args.warmup):
+        graph.replay()
+    graph_ms = timed(graph.replay, Kd)
+
     # the write before a decode step: every sequence's newest token appended
     # (fp16 rows; INT8 with the fused re-quantize of the tail tiles)
     kn, vn, pos = W.append_tokens(w, 99)
@@ -755,6 +765,9 @@ def main():
                            "GB/s": dec_b / (statistics.mean(f8_ms) * 1e-3) / 1e9,
                            "frac_of_peak": dec_b / (statistics.mean(f8_ms) * 1e-3) / 1e9 / peak,
                            "bytes": dec_b},
+            "step_cuda_graph": {"p50_us": 1e3 * statistics.median(graph_ms),
+                                "GB/s": step_b / (statistics.mean(graph_ms) * 1e-3) / 1e9,
+                                "bytes": step_b},
             "quantize_tail_blocks": {"p50_us": 1e3 * statistics.median(q_ms),
                                      "tiles": 2 * ntiles,
                                      "bytes": quantize_bytes(ntiles, d)},
