@@ -62,6 +62,7 @@ PKV_STATIC_WORKSPACE_BYTES = 32 << 20
 
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
 
 
 class BmStats(ctypes.Structure):
@@ -87,57 +88,76 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError(
                 f"libpkv is not built ({LIB_PATH} missing); run "
                 "paged_kv_cache_234_gb300.build.build() first -- there is no fallback")
-        L = ctypes.CDLL(LIB_PATH)
-        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-        L.pkv_quantize_blocks.restype = I
-        L.pkv_quantize_blocks.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P]
-        dec = [P, P, P, P, I, P, I, P, I, I, I, I, I, I, F, P, Z, P, P]
-        L.pkv_paged_decode_fp16.restype = I
-        L.pkv_paged_decode_fp16.argtypes = dec
-        L.pkv_paged_decode_int8.restype = I
-        L.pkv_paged_decode_int8.argtypes = dec[:4] + [P, P] + dec[4:]
-        L.pkv_paged_decode_fp8.restype = I
-        L.pkv_paged_decode_fp8.argtypes = dec[:4] + [P, P] + dec[4:]
-        L.pkv_quantize_blocks_fp8.restype = I
-        L.pkv_quantize_blocks_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P]
-        L.pkv_paged_decode_int8_static_workspace.restype = I
-        L.pkv_paged_decode_int8_static_workspace.argtypes = dec[:4] + [P, P] + dec[4:15] + dec[17:]
-        app = [P, P, I, P, P, P, I, P, I, I, I, I, P, P]
-        L.pkv_append_fp16.restype = I
-        L.pkv_append_fp16.argtypes = app
-        L.pkv_append_int8.restype = I
-        L.pkv_append_int8.argtypes = app[:2] + [P, P, P, P] + app[2:]
-        L.pkv_append_fp8.restype = I
-        L.pkv_append_fp8.argtypes = app[:2] + [P, P, P, P] + app[2:]
-        L.pkv_evict_select.restype = I
-        L.pkv_evict_select.argtypes = [P, P, I, ctypes.c_int64, F, F, I, P, P, P, P]
-        L.pkv_bm_create.restype = I
-        L.pkv_bm_create.argtypes = [I, I, ctypes.POINTER(P)]
-        L.pkv_bm_destroy.restype = None
-        L.pkv_bm_destroy.argtypes = [P]
-        L.pkv_bm_allocate.restype = I
-        L.pkv_bm_allocate.argtypes = [P, P, I, P]
-        for name in ("pkv_bm_free", "pkv_bm_fork"):
-            getattr(L, name).restype = I
-            getattr(L, name).argtypes = [P, P, I]
-        L.pkv_bm_cow.restype = I
-        L.pkv_bm_cow.argtypes = [P, P, I, P, P, ctypes.POINTER(I)]
-        L.pkv_bm_set_fill.restype = I
-        L.pkv_bm_set_fill.argtypes = [P, P, P, I]
-        L.pkv_bm_stats.restype = I
-        L.pkv_bm_stats.argtypes = [P, ctypes.POINTER(BmStats)]
-        L.pkv_bm_refcounts.restype = I
-        L.pkv_bm_refcounts.argtypes = [P, P, I]
-        L.pkv_copy_blocks.restype = I
-        L.pkv_copy_blocks.argtypes = [P, P, I, I, P, I, P, P]
-        L.pkv_decode_workspace_size.restype = Z
-        L.pkv_decode_workspace_size.argtypes = [I, I, I, I, I]
-        L.pkv_set_decode_workers.restype = I
-        L.pkv_set_decode_workers.argtypes = [I]
-        L.pkv_status_string.restype = ctypes.c_char_p
-        L.pkv_status_string.argtypes = [I]
-        _lib = L
-        return L
+        _lib = _declare(ctypes.CDLL(LIB_PATH))
+        return _lib
+
+
+def debug_lib() -> ctypes.CDLL:
+    """The library built with the decode kernel's debug checks
+    (``build.build_debug()``), argument types set, plus ``pkv_debug_flags``.
+    Test support only: the calls of this module always use ``lib()``."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            from . import build as _build
+            L = _declare(ctypes.CDLL(_build.build_debug()))
+            L.pkv_debug_flags.restype = ctypes.c_uint
+            L.pkv_debug_flags.argtypes = [ctypes.c_int]
+            _debug_lib = L
+        return _debug_lib
+
+
+def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Argument and result types of every C ABI entry point on ``L``."""
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.pkv_quantize_blocks.restype = I
+    L.pkv_quantize_blocks.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P]
+    dec = [P, P, P, P, I, P, I, P, I, I, I, I, I, I, F, P, Z, P, P]
+    L.pkv_paged_decode_fp16.restype = I
+    L.pkv_paged_decode_fp16.argtypes = dec
+    L.pkv_paged_decode_int8.restype = I
+    L.pkv_paged_decode_int8.argtypes = dec[:4] + [P, P] + dec[4:]
+    L.pkv_paged_decode_fp8.restype = I
+    L.pkv_paged_decode_fp8.argtypes = dec[:4] + [P, P] + dec[4:]
+    L.pkv_quantize_blocks_fp8.restype = I
+    L.pkv_quantize_blocks_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P]
+    L.pkv_paged_decode_int8_static_workspace.restype = I
+    L.pkv_paged_decode_int8_static_workspace.argtypes = dec[:4] + [P, P] + dec[4:15] + dec[17:]
+    app = [P, P, I, P, P, P, I, P, I, I, I, I, P, P]
+    L.pkv_append_fp16.restype = I
+    L.pkv_append_fp16.argtypes = app
+    L.pkv_append_int8.restype = I
+    L.pkv_append_int8.argtypes = app[:2] + [P, P, P, P] + app[2:]
+    L.pkv_append_fp8.restype = I
+    L.pkv_append_fp8.argtypes = app[:2] + [P, P, P, P] + app[2:]
+    L.pkv_evict_select.restype = I
+    L.pkv_evict_select.argtypes = [P, P, I, ctypes.c_int64, F, F, I, P, P, P, P]
+    L.pkv_bm_create.restype = I
+    L.pkv_bm_create.argtypes = [I, I, ctypes.POINTER(P)]
+    L.pkv_bm_destroy.restype = None
+    L.pkv_bm_destroy.argtypes = [P]
+    L.pkv_bm_allocate.restype = I
+    L.pkv_bm_allocate.argtypes = [P, P, I, P]
+    for name in ("pkv_bm_free", "pkv_bm_fork"):
+        getattr(L, name).restype = I
+        getattr(L, name).argtypes = [P, P, I]
+    L.pkv_bm_cow.restype = I
+    L.pkv_bm_cow.argtypes = [P, P, I, P, P, ctypes.POINTER(I)]
+    L.pkv_bm_set_fill.restype = I
+    L.pkv_bm_set_fill.argtypes = [P, P, P, I]
+    L.pkv_bm_stats.restype = I
+    L.pkv_bm_stats.argtypes = [P, ctypes.POINTER(BmStats)]
+    L.pkv_bm_refcounts.restype = I
+    L.pkv_bm_refcounts.argtypes = [P, P, I]
+    L.pkv_copy_blocks.restype = I
+    L.pkv_copy_blocks.argtypes = [P, P, I, I, P, I, P, P]
+    L.pkv_decode_workspace_size.restype = Z
+    L.pkv_decode_workspace_size.argtypes = [I, I, I, I, I]
+    L.pkv_set_decode_workers.restype = I
+    L.pkv_set_decode_workers.argtypes = [I]
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_status_string.argtypes = [I]
+    return L
 
 
 def pkv_status_string(status: int) -> str:

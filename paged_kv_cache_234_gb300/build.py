@@ -16,6 +16,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libpkv.so")
+DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libpkv_debug.so")
 INCLUDE = os.path.join(os.path.dirname(PKG_DIR), "include")
 SOURCES = ("pkv_host.cu", "pkv_quantize.cu", "pkv_decode.cu", "pkv_append.cu", "pkv_evict.cu",
            "pkv_copy.cu", "pkv_block_manager.cpp")
@@ -71,6 +72,33 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
+
+
+def build_debug() -> str:
+    """libpkv_debug.so: the library with the decode kernel built with
+    PKV_DEBUG (shared-memory address and table-index checks, read back by
+    pkv_debug_flags).  For tests; the release library is untouched."""
+    build()
+    if os.path.exists(DEBUG_LIB_PATH) and all(
+            os.path.getmtime(f) <= os.path.getmtime(DEBUG_LIB_PATH) for f in _inputs()):
+        return DEBUG_LIB_PATH
+    nvcc = _nvcc()
+    obj = os.path.join(BUILD_DIR, "pkv_decode_debug.o")
+    cmd = [nvcc] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                           "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-DPKV_DEBUG",
+                           "-c", os.path.join(CSRC, "pkv_decode.cu"), "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for the debug decode:\n{r.stdout}\n{r.stderr}")
+    objs = [os.path.join(BUILD_DIR, os.path.splitext(f)[0] + ".o") for f in SOURCES
+            if f != "pkv_decode.cu"] + [obj]
+    tmp = DEBUG_LIB_PATH + f".tmp{os.getpid()}"
+    cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lrt", "-ldl", "-lpthread"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, DEBUG_LIB_PATH)
+    return DEBUG_LIB_PATH
 
 
 if __name__ == "__main__":

@@ -89,6 +89,47 @@ struct DecodeArgs {
     float scale_log2;    // softmax_scale * log2(e)
 };
 
+// ------------------------------------------------------ debug build checks
+// Built with PKV_DEBUG, the decode kernel checks every shared-memory address
+// it forms (range inside the CTA's dynamic shared memory, alignment of the
+// access) and every index into its per-sequence tables and the block tables.
+// A failed check sets a bit in g_debug_flags (read by pkv_debug_flags) and the
+// access is redirected to the start of the buffer or to index 0, so nothing
+// outside the buffers is touched.  Release builds compile the checks away.
+#ifdef PKV_DEBUG
+__device__ unsigned int g_debug_flags;
+constexpr unsigned kDbgSmemRange = 1u, kDbgSmemAlign = 2u, kDbgIndex = 4u;
+
+__device__ __forceinline__ uint32_t dbg_smem(uint32_t addr, uint32_t bytes, uint32_t align)
+{
+    extern __shared__ __align__(16) uint8_t dbg_dyn_smem[];
+    const uint32_t lo = static_cast<uint32_t>(__cvta_generic_to_shared(dbg_dyn_smem));
+    uint32_t size;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(size));
+    unsigned bad = 0;
+    if (addr < lo || addr + bytes > lo + size) bad |= kDbgSmemRange;
+    if (addr & (align - 1)) bad |= kDbgSmemAlign;
+    if (!bad) return addr;
+    atomicOr(&g_debug_flags, bad);
+    return (lo + align - 1) & ~(align - 1);
+}
+
+__device__ __forceinline__ int64_t dbg_index(int64_t i, int64_t n)
+{
+    if (i >= 0 && i < n) return i;
+    atomicOr(&g_debug_flags, kDbgIndex);
+    return 0;
+}
+#define PKV_SMEM(addr, bytes, align) dbg_smem((addr), (bytes), (align))
+#define PKV_IDX(i, n) dbg_index((i), (n))
+#define PKV_TABLE_AT(p, seq, page, u, mb) \
+    ((p).block_tables + dbg_index((seq), (p).num_seqs) * (mb) + dbg_index((page) + (u), (mb)))
+#else
+#define PKV_SMEM(addr, bytes, align) (addr)
+#define PKV_IDX(i, n) (i)
+#define PKV_TABLE_AT(p, seq, page, u, mb) ((p).block_tables + (seq) * (mb) + (page) + (u))
+#endif
+
 // Pipeline shape per variant: pages per stage, stages per warp, CTAs (of
 // four warps) per SM.  Shared memory per CTA is 4 * stages * pages * (K + V
 // tile) bytes; the register budget follows from the CTA count.
@@ -240,13 +281,13 @@ struct PageCursor {
         int lo = 0, hi = p.num_seqs;  // largest s with items_per_seq * prefix[s] <= x
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (static_cast<int64_t>(p.items_per_seq) * prefix[mid] <= x)
+            if (static_cast<int64_t>(p.items_per_seq) * prefix[PKV_IDX(mid, p.num_seqs + 1)] <= x)
                 lo = mid;
             else
                 hi = mid;
         }
         seq = lo;
-        npages = prefix[lo + 1] - prefix[lo];
+        npages = prefix[PKV_IDX(lo + 1, p.num_seqs + 1)] - prefix[lo];
         const int64_t r = x - static_cast<int64_t>(p.items_per_seq) * prefix[lo];
         item = static_cast<int>(r / npages);
         page = static_cast<int>(r % npages);
@@ -334,7 +375,7 @@ __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             uint32_t a0, a1, a2, a3;
-            ptx::ldsm_x4(kt + swz<C::kRowBytes>(lt, 2 * ks + lch), a0, a1, a2, a3);
+            ptx::ldsm_x4(PKV_SMEM(kt + swz<C::kRowBytes>(lt, 2 * ks + lch), 16, 16), a0, a1, a2, a3);
             if (ks & 1)
                 ptx::mma_16816(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             else
@@ -352,7 +393,8 @@ __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD
         for (int r = 0; r < 2; ++r) {
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
-                const uint4 v = ptx::lds128(kt + swz<C::kRowBytes>(g + 8 * r, CH * c + j));
+                const uint4 v =
+                    ptx::lds128(PKV_SMEM(kt + swz<C::kRowBytes>(g + 8 * r, CH * c + j), 16, 16));
                 kw[r][4 * j + 0] = v.x ^ kFlip;
                 kw[r][4 * j + 1] = v.y ^ kFlip;
                 kw[r][4 * j + 2] = v.z ^ kFlip;
@@ -403,7 +445,7 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
 #pragma unroll
         for (int i = 0; i < KS; ++i) {
             uint32_t a0, a1, a2, a3;
-            ptx::ldsm_x4_t(vt + swz<C::kRowBytes>(lt, 2 * i + lch), a0, a1, a2, a3);
+            ptx::ldsm_x4_t(PKV_SMEM(vt + swz<C::kRowBytes>(lt, 2 * i + lch), 16, 16), a0, a1, a2, a3);
             ptx::mma_16816(o[i], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
         }
     } else {
@@ -415,13 +457,14 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
         for (int r = 0; r < 4; ++r) {
             const int t = 2 * c + (r & 1) + 8 * (r >> 1);
             if constexpr (kD == 128) {
-                const uint4 v = ptx::lds128(vt + swz<C::kRowBytes>(t, g));
+                const uint4 v = ptx::lds128(PKV_SMEM(vt + swz<C::kRowBytes>(t, g), 16, 16));
                 vw[r][0] = v.x ^ kFlip;
                 vw[r][1] = v.y ^ kFlip;
                 vw[r][2] = v.z ^ kFlip;
                 vw[r][3] = v.w ^ kFlip;
             } else {
-                const uint2 v = ptx::lds64(vt + swz<C::kRowBytes>(t, g >> 1) + (g & 1) * 8);
+                const uint2 v =
+                    ptx::lds64(PKV_SMEM(vt + swz<C::kRowBytes>(t, g >> 1) + (g & 1) * 8, 8, 8));
                 vw[r][0] = v.x ^ kFlip;
                 vw[r][1] = v.y ^ kFlip;
             }
@@ -462,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     constexpr int S = C::kStages;
     constexpr int PPS = C::kPPS;
     constexpr int KS = kD / 16;  // mma k-steps over head_dim, also m-tiles of O^T
+    [[maybe_unused]] constexpr uint32_t kTmaAlign = C::kSwizzle == 128 ? 1024 : 512;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -506,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     const uint32_t hdr0 = ptx::smem_addr(hdr_base);
     const uint32_t bar0 = ptx::smem_addr(smem + C::kBarOffset) + warp * S * 8;
     if (lane == 0) {
-        for (int s = 0; s < S; ++s) ptx::mbar_init(bar0 + 8 * s, kInt8 ? 2 : 1);
+        for (int s = 0; s < S; ++s) ptx::mbar_init(PKV_SMEM(bar0 + 8 * s, 8, 8), kInt8 ? 2 : 1);
         ptx::fence_mbar_init();
     }
     __syncwarp();
@@ -526,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             if (u < cnt && !ok && p.dev_status) atomicOr(p.dev_status, PKV_DEV_BAD_BLOCK);
             bytes += ok ? C::kPageBytes : 0;
         }
-        ptx::mbar_arrive_expect_tx(bar, bytes);
+        ptx::mbar_arrive_expect_tx(PKV_SMEM(bar, 8, 8), bytes);
 #pragma unroll
         for (int u = 0; u < PPS; ++u) {
             if (hb[u]) continue;
@@ -534,18 +578,23 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             const uint32_t kdst = stage0 + slot * C::kStageBytes + u * C::kPageBytes;
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
-                ptx::tma_load_2d(kdst + bx * C::kBoxBytes, &tmk, bx * C::kBoxInner, row, bar,
+                ptx::tma_load_2d(PKV_SMEM(kdst + bx * C::kBoxBytes, C::kBoxBytes, kTmaAlign), &tmk,
+                                 bx * C::kBoxInner, row, bar,
                                  policy);
-                ptx::tma_load_2d(kdst + C::kTileBytes + bx * C::kBoxBytes, &tmv,
+                ptx::tma_load_2d(PKV_SMEM(kdst + C::kTileBytes + bx * C::kBoxBytes, C::kBoxBytes,
+                                          kTmaAlign),
+                                 &tmv,
                                  bx * C::kBoxInner, row, bar, policy);
             }
             if constexpr (kInt8) {
                 const int64_t si = static_cast<int64_t>(blk[u]) * p.num_kv_heads + kvh;
-                ptx::cp_async_4(hdr0 + slot * C::kHdrBytes + 8 + 4 * u, p.k_scales + si);
-                ptx::cp_async_4(hdr0 + slot * C::kHdrBytes + 16 + 4 * u, p.v_scales + si);
+                ptx::cp_async_4(PKV_SMEM(hdr0 + slot * C::kHdrBytes + 8 + 4 * u, 4, 4),
+                                p.k_scales + si);
+                ptx::cp_async_4(PKV_SMEM(hdr0 + slot * C::kHdrBytes + 16 + 4 * u, 4, 4),
+                                p.v_scales + si);
             }
         }
-        if constexpr (kInt8) ptx::cp_async_arrive_noinc(bar);
+        if constexpr (kInt8) ptx::cp_async_arrive_noinc(PKV_SMEM(bar, 8, 8));
     };
 
     // ---- prologue: block ids of the first stages (one lane per page), issue
@@ -566,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             if (j == my_stage) {
                 mycnt = cnt;
                 mykvh = cj.kvh;
-                if (my_u < cnt) myblk = __ldg(p.block_tables + cj.seq * mb + cj.page + my_u);
+                if (my_u < cnt) myblk = __ldg(PKV_TABLE_AT(p, cj.seq, cj.page, my_u, mb));
             }
             cj.advance(p, prefix, cnt);
             pos += cnt;
@@ -586,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     // lanes u < PPS: block id of page u of the next stage to issue
     int32_t nblk = 0;
     if (ipos < n && lane < ci.unit(PPS, n - ipos))
-        nblk = __ldg(p.block_tables + ci.seq * mb + ci.page + lane);
+        nblk = __ldg(PKV_TABLE_AT(p, ci.seq, ci.page, lane, mb));
 
     // ---- per-piece state
     float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 units), heads 2c and 2c+1
@@ -660,13 +709,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
         piece_pages += cnt;
 
         // every lane waits (acquire); the outcome is made warp-uniform
-        const bool landed = ptx::mbar_wait_bounded(bar0 + 8 * slot, parity, kWaitLimitNs);
+        const bool landed =
+            ptx::mbar_wait_bounded(PKV_SMEM(bar0 + 8 * slot, 8, 8), parity, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, landed)) {
             // The copy never landed: report, let this worker's other copies
             // land (bounded), and stop this worker.
             if (lane == 0 && p.dev_status) atomicOr(p.dev_status, PKV_DEV_TIMEOUT);
             for (uint32_t r = k + 1; r < issued; ++r)
-                ptx::mbar_wait_bounded(bar0 + 8 * (r % S), (r / S) & 1u, kWaitLimitNs);
+                ptx::mbar_wait_bounded(PKV_SMEM(bar0 + 8 * (r % S), 8, 8), (r / S) & 1u,
+                                       kWaitLimitNs);
             return;
         }
 
@@ -682,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
         }
         if (any_good) {
             const uint32_t st = stage0 + slot * C::kStageBytes;
-            const int ctx = ctxs[cc.seq];
+            const int ctx = ctxs[PKV_IDX(cc.seq, p.num_seqs)];
             // ---- scores of the stage's pages, base-2 logits
             float x[PPS][4];
 #pragma unroll
@@ -782,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             ipos += icnt;
             ++issued;
             if (ipos < n && lane < ci.unit(PPS, n - ipos))
-                nblk = __ldg(p.block_tables + ci.seq * mb + ci.page + lane);
+                nblk = __ldg(PKV_TABLE_AT(p, ci.seq, ci.page, lane, mb));
         }
 
         // ---- piece finished: final output, or a partial for the reduce
@@ -826,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             }
             if (!whole && piece_first_page == 0 && lane == 0) {
                 // this piece starts an item that later workers continue
-                const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[cc.seq] +
+                const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[PKV_IDX(cc.seq, p.num_seqs)] +
                                    static_cast<int64_t>(cc.item) * cc.npages;
                 write_split(p, w, true, piece_has_a ? 0 : 1,
                             worker_of(s0 + cc.npages - 1, total, p.num_workers), cc.seq, cc.item,
@@ -1326,3 +1377,22 @@ extern "C" pkv_status pkv_paged_decode_int8_static_workspace(
     // rejected with PKV_ERR_WORKSPACE before anything is launched
     return pkv::decode_entry(call, pkv::kKvI8);
 }
+
+#ifdef PKV_DEBUG
+// Debug builds only (not part of the C ABI header): the OR of the check bits
+// set since the last reset (1: a shared-memory address outside the dynamic
+// shared memory, 2: a misaligned one, 4: a table index out of range); reset
+// nonzero clears them.  Synchronises with the device.
+extern "C" __attribute__((visibility("default"))) unsigned int pkv_debug_flags(int reset)
+{
+    unsigned int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&v, pkv::g_debug_flags, sizeof(v)) != cudaSuccess)
+        return 0xffffffffu;
+    if (reset) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(pkv::g_debug_flags, &z, sizeof(z)) != cudaSuccess) return 0xffffffffu;
+    }
+    return v;
+}
+#endif
