@@ -101,8 +101,9 @@ def debug_lib() -> ctypes.CDLL:
         if _debug_lib is None:
             from . import build as _build
             L = _declare(ctypes.CDLL(_build.build_debug()))
-            L.pkv_debug_flags.restype = ctypes.c_uint
-            L.pkv_debug_flags.argtypes = [ctypes.c_int]
+            for name in ("pkv_debug_flags", "pkv_debug_evict_flags"):
+                getattr(L, name).restype = ctypes.c_uint
+                getattr(L, name).argtypes = [ctypes.c_int]
             _debug_lib = L
         return _debug_lib
 

@@ -74,24 +74,34 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB_PATH
 
 
+DEBUG_SOURCES = ("pkv_decode.cu", "pkv_evict.cu")  # the kernels with PKV_DEBUG checks
+
+
 def build_debug() -> str:
-    """libpkv_debug.so: the library with the decode kernel built with
-    PKV_DEBUG (shared-memory address and table-index checks, read back by
-    pkv_debug_flags).  For tests; the release library is untouched."""
+    """libpkv_debug.so: the library with the decode and eviction kernels built
+    with PKV_DEBUG (shared-memory address and index checks, read back by
+    pkv_debug_flags / pkv_debug_evict_flags).  For tests; the release library
+    is untouched."""
     build()
     if os.path.exists(DEBUG_LIB_PATH) and all(
             os.path.getmtime(f) <= os.path.getmtime(DEBUG_LIB_PATH) for f in _inputs()):
         return DEBUG_LIB_PATH
     nvcc = _nvcc()
-    obj = os.path.join(BUILD_DIR, "pkv_decode_debug.o")
-    cmd = [nvcc] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                           "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-DPKV_DEBUG",
-                           "-c", os.path.join(CSRC, "pkv_decode.cu"), "-o", obj]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed for the debug decode:\n{r.stdout}\n{r.stderr}")
+
+    def compile_debug(src):
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + "_debug.o")
+        cmd = [nvcc] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-DPKV_DEBUG",
+                               "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for the debug {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with concurrent.futures.ThreadPoolExecutor(len(DEBUG_SOURCES)) as ex:
+        dbg = list(ex.map(compile_debug, DEBUG_SOURCES))
     objs = [os.path.join(BUILD_DIR, os.path.splitext(f)[0] + ".o") for f in SOURCES
-            if f != "pkv_decode.cu"] + [obj]
+            if f not in DEBUG_SOURCES] + dbg
     tmp = DEBUG_LIB_PATH + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lrt", "-ldl", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -114,6 +114,29 @@ __device__ __forceinline__ uint32_t bins_exclusive_scan(uint32_t v, uint32_t *pa
     return before + x - v;
 }
 
+// Built with PKV_DEBUG: the slice this CTA stages must fit its dynamic shared
+// memory, the cluster must fit the per-CTA peer arrays, and every 16-byte
+// copy destination must lie inside the slice buffers; a failed check sets a
+// bit in g_ev_debug_flags (read by pkv_debug_evict_flags) and the CTA takes
+// an empty slice / skips the copy instead.  Release builds compile it away.
+#ifdef PKV_DEBUG
+__device__ unsigned int g_ev_debug_flags;
+__device__ __forceinline__ bool ev_dbg_ok(bool ok, unsigned bit)
+{
+    if (!ok) atomicOr(&g_ev_debug_flags, bit);
+    return ok;
+}
+__device__ __forceinline__ uint32_t ev_dyn_smem_size()
+{
+    uint32_t r;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+#define PKV_EV_CHECK(cond, bit) ev_dbg_ok((cond), (bit))
+#else
+#define PKV_EV_CHECK(cond, bit) true
+#endif
+
 __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
 {
     extern __shared__ __align__(16) unsigned char ev_smem[];
@@ -133,7 +156,14 @@ __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t lo = static_cast<int64_t>(rank) * p.slice;
     const int64_t left = static_cast<int64_t>(p.num_blocks) - lo;
-    const int n_local = static_cast<int>(left < 0 ? 0 : (left < p.slice ? left : p.slice));
+    int n_local = static_cast<int>(left < 0 ? 0 : (left < p.slice ? left : p.slice));
+#ifdef PKV_DEBUG
+    // the slice buffers (keys; ages when staged) inside the dynamic shared
+    // memory, the cluster within the peer arrays
+    if (!PKV_EV_CHECK(static_cast<uint64_t>(p.slice) * (p.staged ? 12u : 4u) <= ev_dyn_smem_size(), 1u) ||
+        !PKV_EV_CHECK(csize <= static_cast<uint32_t>(kEvMaxCluster) && rank < csize, 2u))
+        n_local = 0;
+#endif
     const long long *last_used = reinterpret_cast<const long long *>(p.last_used) + lo;
     for (int b = tid; b < kEvWarps * kEvBins; b += kEvThreads) (&warp_hist[0][0])[b] = 0;
     if (tid < kEvBins) {
@@ -148,9 +178,11 @@ __global__ void __launch_bounds__(kEvThreads, 1) evict_kernel(EvictParams p)
     if (p.staged) {
         const int nr = n_local >> 2, na = n_local >> 1;  // 16-byte chunks
         for (int c = tid; c < nr; c += kEvThreads)
-            ptx::cp_async_16(ptx::smem_addr(keys + 4 * c), refcnt + 4 * c);
+            if (PKV_EV_CHECK(4 * c + 4 <= p.slice, 4u))
+                ptx::cp_async_16(ptx::smem_addr(keys + 4 * c), refcnt + 4 * c);
         for (int c = tid; c < na; c += kEvThreads)
-            ptx::cp_async_16(ptx::smem_addr(ages + 2 * c), last_used + 2 * c);
+            if (PKV_EV_CHECK(2 * c + 2 <= p.slice, 4u))
+                ptx::cp_async_16(ptx::smem_addr(ages + 2 * c), last_used + 2 * c);
         if (tid == 0) {
             for (int j = 4 * nr; j < n_local; ++j) keys[j] = static_cast<uint32_t>(__ldg(refcnt + j));
             for (int j = 2 * na; j < n_local; ++j) ages[j] = __ldg(last_used + j);
@@ -446,3 +478,22 @@ extern "C" pkv_status pkv_evict_select(const int32_t *refcnt, const int64_t *las
     }
     return PKV_OK;
 }
+
+#ifdef PKV_DEBUG
+// Debug builds only (not part of the C ABI header): the eviction kernel's
+// check bits set since the last reset (1: slice larger than the dynamic
+// shared memory, 2: cluster larger than the peer arrays, 4: a copy outside
+// the slice); reset nonzero clears them.  Synchronises with the device.
+extern "C" __attribute__((visibility("default"))) unsigned int pkv_debug_evict_flags(int reset)
+{
+    unsigned int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&v, pkv::g_ev_debug_flags, sizeof(v)) != cudaSuccess)
+        return 0xffffffffu;
+    if (reset) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(pkv::g_ev_debug_flags, &z, sizeof(z)) != cudaSuccess) return 0xffffffffu;
+    }
+    return v;
+}
+#endif

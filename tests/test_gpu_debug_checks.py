@@ -1,10 +1,14 @@
-"""The decode kernel built with its debug checks (PKV_DEBUG): every
-shared-memory address it forms stays inside the CTA's dynamic shared memory
-and is aligned for its access, and every table index is in range, on a spread
-of shapes -- head dims 64 and 128, group sizes 1 to 16, ragged and edge
-lengths, one item split over many workers, the largest batch -- with the
-outputs still matching the oracle.  A failed check would redirect the access
-in bounds and set a flag, so these runs cannot fault.
+"""The decode and eviction kernels built with their debug checks (PKV_DEBUG).
+
+Decode: every shared-memory address it forms stays inside the CTA's dynamic
+shared memory and is aligned for its access, and every table index is in
+range, on a spread of shapes -- head dims 64 and 128, group sizes 1 to 16,
+ragged and edge lengths, one item split over many workers, 3000 sequences --
+with the outputs still matching the oracle.  Eviction: each CTA's staged
+slice fits its shared memory, the cluster fits the peer arrays and every
+16-byte copy lands inside the slice, from 1 block to the largest pool one
+launch takes, with the oracle's choice.  A failed check redirects or skips
+the access and sets a flag, so these runs cannot fault.
 """
 import numpy as np
 import pytest
@@ -85,3 +89,36 @@ def test_debug_build_finds_no_out_of_range_access(L, name, kw, workers, variant)
     ref, oflags = oracle_decode(w, variant, codes)
     assert st == 0 and not oflags.any()
     assert_close(got, ref, f"{name}/{variant} (debug build)")
+
+
+@pytest.mark.parametrize("num_blocks", [1, 100, 1024, 16384, 65536, 200_000, 16 * 49152])
+def test_debug_build_eviction_stays_in_its_buffers(L, num_blocks):
+    import oracle
+    if num_blocks == 16 * 49152:
+        # the largest pool one launch takes: 16-CTA clusters where the
+        # device schedules them, else 8
+        probe_ref = torch.zeros(num_blocks, dtype=torch.int32, device="cuda")
+        probe_last = torch.zeros(num_blocks, dtype=torch.int64, device="cuda")
+        cnt0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if L.pkv_evict_select(probe_ref.data_ptr(), probe_last.data_ptr(), num_blocks, 0, 0.7,
+                              0.3, 0, None, None, cnt0.data_ptr(),
+                              torch.cuda.current_stream().cuda_stream) == pkv.PKV_ERR_UNSUPPORTED:
+            num_blocks = 8 * 49152
+        torch.cuda.synchronize()
+    k = pkv.evict_count(num_blocks) or 1
+    st = W.eviction_state(num_blocks, 31)
+    ref, last = dev(st.refcnt), dev(st.last_used)
+    ids = torch.empty(max(k, 1), dtype=torch.int32, device="cuda")
+    cnt = torch.empty(1, dtype=torch.int32, device="cuda")
+    sc = torch.empty(num_blocks, dtype=torch.float32, device="cuda")
+    L.pkv_debug_evict_flags(1)
+    rc = L.pkv_evict_select(ref.data_ptr(), last.data_ptr(), num_blocks, st.current_tick,
+                            pkv.EVICT_ALPHA, pkv.EVICT_BETA, k, sc.data_ptr(), ids.data_ptr(),
+                            cnt.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    flags = L.pkv_debug_evict_flags(1)
+    assert flags == 0, f"eviction debug check bits {flags:#x}"
+    want_ids, want_sc = oracle.evict_select(st.refcnt, st.last_used, st.current_tick, k)
+    assert int(cnt.item()) == want_ids.size
+    assert np.array_equal(ids.cpu().numpy()[: want_ids.size], want_ids)
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), want_sc.view(np.uint32))
