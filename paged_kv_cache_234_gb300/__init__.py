@@ -104,6 +104,8 @@ def debug_lib() -> ctypes.CDLL:
             for name in ("pkv_debug_flags", "pkv_debug_evict_flags"):
                 getattr(L, name).restype = ctypes.c_uint
                 getattr(L, name).argtypes = [ctypes.c_int]
+            L.pkv_debug_set_stage_wait_ns.restype = ctypes.c_int
+            L.pkv_debug_set_stage_wait_ns.argtypes = [ctypes.c_longlong]
             _debug_lib = L
         return _debug_lib
 

@@ -38,8 +38,17 @@
 // INT8 codes are widened to f16 exactly by byte permutes: a code c placed
 // under the exponent byte 0x64 reads as 1152 + c.  For K the constant 1152
 // is left in and removed from the scores as 1152 * sum(q); for V it is
-// subtracted before the product.  The K scale multiplies the scores and the
-// V scale the probabilities.
+// subtracted before the product.  The K scale multiplies the scores.  The V
+// scale enters as a ratio to the piece's largest V scale so far (<= 1, the
+// accumulators move to a new reference with the softmax rescale), and the
+// reference multiplies the accumulators when they leave the registers, so
+// the result does not depend on the magnitude of V.
+//
+// The probabilities (times 2^15, times the V scale ratio) reach the PV mma as
+// fp32 values: an f16 high part plus an f16 low part (the next 11 bits),
+// either in the spare mma columns (groups of up to four query heads) or as a
+// second mma into the same accumulators.  So P is not rounded to f16
+// precision, and differently split batches agree to float rounding.
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -62,6 +71,8 @@ constexpr int kMaxWorkersPerItem = 4;  // measured on GB300: 8 x 512, 32 x 1024 
                                        // worker per resident warp
 constexpr int kMaxSeqs = 8192;         // per-sequence tables live in shared memory
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
+constexpr float kPScale = 32768.f;     // probabilities enter PV as 2^15 p (see the main loop)
+constexpr float kPScaleInv = 1.f / 32768.f;
 
 int g_worker_cap = 0;  // pkv_set_decode_workers
 std::mutex g_cfg_mu;
@@ -120,11 +131,18 @@ __device__ __forceinline__ int64_t dbg_index(int64_t i, int64_t n)
     atomicOr(&g_debug_flags, kDbgIndex);
     return 0;
 }
+// Limit of the main loop's waits for a stage (the drain after a timeout keeps
+// kWaitLimitNs).  Settable through pkv_debug_set_stage_wait_ns so that a test
+// can make a wait run out on a copy that does land: 0 means a wait that gives
+// up at once, as if its limit had run out.
+__device__ unsigned long long g_debug_stage_wait_ns = kWaitLimitNs;
+#define PKV_STAGE_WAIT_NS g_debug_stage_wait_ns
 #define PKV_SMEM(addr, bytes, align) dbg_smem((addr), (bytes), (align))
 #define PKV_IDX(i, n) dbg_index((i), (n))
 #define PKV_TABLE_AT(p, seq, page, u, mb) \
     ((p).block_tables + dbg_index((seq), (p).num_seqs) * (mb) + dbg_index((page) + (u), (mb)))
 #else
+#define PKV_STAGE_WAIT_NS kWaitLimitNs
 #define PKV_SMEM(addr, bytes, align) (addr)
 #define PKV_IDX(i, n) (i)
 #define PKV_TABLE_AT(p, seq, page, u, mb) ((p).block_tables + (seq) * (mb) + (page) + (u))
@@ -327,6 +345,11 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+__device__ __forceinline__ float2 unpack_half2(uint32_t w)
+{
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+
 // two int8 codes (bytes picked by sel from a word already XOR-ed with 0x80)
 // as an f16 pair 1152 + c, exact
 __device__ __forceinline__ uint32_t i8pair_biased(uint32_t xw, uint32_t sel)
@@ -426,9 +449,16 @@ __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD
 }
 
 // O^T += V_page^T . P^T for one page; tokens >= ntok contribute nothing.
-template <int kKv, int kD>
-__device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1, int ntok,
-                                        int lane, float (&o)[kD / 16][4])
+// kLoCols: P^T (pb0, pb1) holds the high f16 parts of the probabilities in
+// columns 0-3 and the low parts in columns 4-7, one mma per k-step.
+// Otherwise P^T arrives as two f16 operands whose sum is the fp32
+// probabilities (high part pb0/pb1, low part pl0/pl1) and both products go
+// into the same fp32 accumulators.  Either way P is not rounded to f16
+// precision.
+template <int kKv, int kD, bool kLoCols>
+__device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1, uint32_t pl0,
+                                        uint32_t pl1, int ntok, int lane,
+                                        float (&o)[kD / 16][4])
 {
     using C = Cfg<kKv, kD>;
     constexpr bool kInt8 = C::kInt8;
@@ -446,7 +476,12 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
         for (int i = 0; i < KS; ++i) {
             uint32_t a0, a1, a2, a3;
             ptx::ldsm_x4_t(PKV_SMEM(vt + swz<C::kRowBytes>(lt, 2 * i + lch), 16, 16), a0, a1, a2, a3);
-            ptx::mma_16816(o[i], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+            a0 &= mlo;
+            a1 &= mlo;
+            a2 &= mhi;
+            a3 &= mhi;
+            ptx::mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
+            if constexpr (!kLoCols) ptx::mma_16816(o[i], a0, a1, a2, a3, pl0, pl1);
         }
     } else {
         // lane (g, c): tokens 2c, 2c+1, 2c+8, 2c+9; bytes [DG*g, DG*g + DG), DG = kD/8
@@ -481,21 +516,31 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
             const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
             const uint32_t il01 = ptx::prmt(vw[0][i >> 1], vw[1][i >> 1], sel);
             const uint32_t il23 = ptx::prmt(vw[2][i >> 1], vw[3][i >> 1], sel);
+            uint32_t a0, a1, a2, a3;
             if constexpr (kKv == kKvI8) {
-                ptx::mma_16816(o[i], i8pair_exact(il01, 0x4140u), i8pair_exact(il01, 0x4342u),
-                               i8pair_exact(il23, 0x4140u), i8pair_exact(il23, 0x4342u), pb0,
-                               pb1);
+                a0 = i8pair_exact(il01, 0x4140u);
+                a1 = i8pair_exact(il01, 0x4342u);
+                a2 = i8pair_exact(il23, 0x4140u);
+                a3 = i8pair_exact(il23, 0x4342u);
             } else {
-                ptx::mma_16816(o[i], ptx::e4m3x2_to_f16x2(il01) & mlo,
-                               ptx::e4m3x2_to_f16x2(il01 >> 16) & mlo,
-                               ptx::e4m3x2_to_f16x2(il23) & mhi,
-                               ptx::e4m3x2_to_f16x2(il23 >> 16) & mhi, pb0, pb1);
+                a0 = ptx::e4m3x2_to_f16x2(il01) & mlo;
+                a1 = ptx::e4m3x2_to_f16x2(il01 >> 16) & mlo;
+                a2 = ptx::e4m3x2_to_f16x2(il23) & mhi;
+                a3 = ptx::e4m3x2_to_f16x2(il23 >> 16) & mhi;
             }
+            ptx::mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
+            if constexpr (!kLoCols) ptx::mma_16816(o[i], a0, a1, a2, a3, pl0, pl1);
         }
     }
 }
 
-template <int kKv, int kD>
+// kLoCols (groups of at most four query heads): mma columns 4-7 repeat the
+// query heads of columns 0-3, so their scores, maxima and probabilities are
+// the same numbers; lanes holding columns 0-3 pass the high f16 part of each
+// probability to PV and lanes holding columns 4-7 the low part, and the two
+// column halves of O^T are added when a piece ends.  Larger groups use all
+// eight columns and a second PV mma for the low parts.
+template <int kKv, int kD, bool kLoCols>
 __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv)
@@ -513,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     int32_t *ctxs = prefix + p.num_seqs + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;  // mma fragment row group / column pair
+    [[maybe_unused]] const float lo_sel = c >= 2 ? 1.f : 0.f;  // kLoCols: low-part lanes
 
     if (threadIdx.x == 0) {
         ptx::prefetch_tmap(&tmk);
@@ -556,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     __syncwarp();
     const uint64_t policy = ptx::policy_evict_first();
     const int64_t mb = p.max_blocks_per_seq;
+    const uint64_t stage_wait_ns = PKV_STAGE_WAIT_NS;
 
     // Lane 0: start the copies of the `cnt` pages of one stage; blk[u] are
     // their block ids, kvh the kv head of the item.
@@ -643,6 +690,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     float o[KS][4];                        // O^T accumulators (see the output mapping)
     uint32_t qf[KS][2];                    // Q^T B-fragments
     float qb0 = 0.f, qb1 = 0.f;            // INT8: 1152 * sum(q) of heads 2c, 2c+1
+    // Codes: V scale reference of the piece (the largest V scale of its pages
+    // so far) and its reciprocal.  A page enters PV with its probabilities
+    // times sv / vref <= 1, so the f16 operand keeps its full precision
+    // whatever the magnitude of V; vref multiplies the accumulators only
+    // when they leave the registers.
+    float vref = 0.f, vinv = 0.f;
     bool piece_bad = false;
     bool piece_has_a = true;
     int piece_first_page = 0;
@@ -659,10 +712,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
         const int gh = min(kItemHeads, p.group - cc.qg * kItemHeads);
 
         if (first) {
-            // query fragments of the item's heads; heads past gh are zero
+            // query fragments of the item's heads (column g: head g, or head
+            // g mod 4 with kLoCols); heads past gh are zero
+            const int hq = kLoCols ? (g & 3) : g;
             const __half *qrow =
-                p.query + (static_cast<int64_t>(cc.seq) * p.num_heads + h0 + g) * kD;
-            const bool live = g < gh;
+                p.query + (static_cast<int64_t>(cc.seq) * p.num_heads + h0 + hq) * kD;
+            const bool live = hq < gh;
             if constexpr (kInt8) {
                 // lane (g, c) holds q[g][DG*c .. DG*c + DG), DG = kD / 4
                 constexpr int DG = kD / 4;
@@ -699,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             }
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
+            vref = vinv = 0.f;
 #pragma unroll
             for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             piece_bad = false;
@@ -710,12 +766,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
 
         // every lane waits (acquire); the outcome is made warp-uniform
         const bool landed =
-            ptx::mbar_wait_bounded(PKV_SMEM(bar0 + 8 * slot, 8, 8), parity, kWaitLimitNs);
+            stage_wait_ns != 0 &&
+            ptx::mbar_wait_bounded(PKV_SMEM(bar0 + 8 * slot, 8, 8), parity, stage_wait_ns);
         if (!__all_sync(0xffffffffu, landed)) {
-            // The copy never landed: report, let this worker's other copies
-            // land (bounded), and stop this worker.
+            // The copy did not land in time: report, let every copy this
+            // worker issued land (bounded; the stage just waited on
+            // included), so that none still writes into this CTA's shared
+            // memory, and stop this worker.
             if (lane == 0 && p.dev_status) atomicOr(p.dev_status, PKV_DEV_TIMEOUT);
-            for (uint32_t r = k + 1; r < issued; ++r)
+            for (uint32_t r = k; r < issued; ++r)
                 ptx::mbar_wait_bounded(PKV_SMEM(bar0 + 8 * (r % S), 8, 8), (r / S) & 1u,
                                        kWaitLimitNs);
             return;
@@ -779,6 +838,26 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             const float al0 = ptx::ex2(m0 - mn0), al1 = ptx::ex2(m1 - mn1);
             m0 = mn0;
             m1 = mn1;
+            float oa0 = al0, oa1 = al1;  // rescale of the accumulators
+            [[maybe_unused]] float vr[PPS];
+            if constexpr (kInt8) {
+                // a page with a larger V scale becomes the reference: the
+                // accumulators move to the new reference with the rescale
+                float smax = vref;
+#pragma unroll
+                for (int u = 0; u < PPS; ++u)
+                    if (good[u]) smax = fmaxf(smax, hf[4 + u]);
+                if (smax > vref) {
+                    vinv = __frcp_rn(smax);
+                    const float ratio = vref * vinv;
+                    vinv *= kPScale;
+                    oa0 *= ratio;
+                    oa1 *= ratio;
+                    vref = smax;
+                }
+#pragma unroll
+                for (int u = 0; u < PPS; ++u) vr[u] = hf[4 + u] * vinv;
+            }
             float pr[PPS][4];
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
@@ -792,28 +871,44 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             }
             l0 = l0 * al0 + ps0;
             l1 = l1 * al1 + ps1;
-            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+            if (__any_sync(0xffffffffu, oa0 != 1.f || oa1 != 1.f)) {
 #pragma unroll
                 for (int i = 0; i < KS; ++i) {
-                    o[i][0] *= al0;
-                    o[i][1] *= al1;
-                    o[i][2] *= al0;
-                    o[i][3] *= al1;
+                    o[i][0] *= oa0;
+                    o[i][1] *= oa1;
+                    o[i][2] *= oa0;
+                    o[i][3] *= oa1;
                 }
             }
             // ---- O^T += V^T . P^T per page (P^T: transposed 8x8 halves of P)
 #pragma unroll
             for (int u = 0; u < PPS; ++u) {
                 if (good[u]) {
-                    float sv = 1.f;
-                    if constexpr (kInt8) sv = hf[4 + u];
-                    const uint32_t pb0 =
-                        ptx::movmatrix_t(pack_half2(pr[u][0] * sv, pr[u][1] * sv));
-                    const uint32_t pb1 =
-                        ptx::movmatrix_t(pack_half2(pr[u][2] * sv, pr[u][3] * sv));
+                    // P' = 2^15 p (codes: 2^15 p sv / vref) <= 2^15, exact
+                    // scaling by a power of two; its f16 high part is a normal
+                    // number down to p = 2^-29 and the low part adds the
+                    // next 11 bits
+                    const float sc = kInt8 ? vr[u] : kPScale;
+                    const float pa = pr[u][0] * sc, pb = pr[u][1] * sc;
+                    const float pc = pr[u][2] * sc, pd = pr[u][3] * sc;
+                    const uint32_t h01 = pack_half2(pa, pb), h23 = pack_half2(pc, pd);
+                    const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
+                    uint32_t pb0, pb1, pl0 = 0, pl1 = 0;
+                    if constexpr (kLoCols) {
+                        // columns 0-3 (c < 2): high parts; 4-7: low parts
+                        pb0 = ptx::movmatrix_t(
+                            pack_half2(fmaf(-lo_sel, f01.x, pa), fmaf(-lo_sel, f01.y, pb)));
+                        pb1 = ptx::movmatrix_t(
+                            pack_half2(fmaf(-lo_sel, f23.x, pc), fmaf(-lo_sel, f23.y, pd)));
+                    } else {
+                        pb0 = ptx::movmatrix_t(h01);
+                        pb1 = ptx::movmatrix_t(h23);
+                        pl0 = ptx::movmatrix_t(pack_half2(pa - f01.x, pb - f01.y));
+                        pl1 = ptx::movmatrix_t(pack_half2(pc - f23.x, pd - f23.y));
+                    }
                     const int ntok = min(kPage, ctx - (cc.page + u) * kPage);
-                    page_pv<kKv, kD>(st + u * C::kPageBytes + C::kTileBytes, pb0, pb1, ntok,
-                                       lane, o);
+                    page_pv<kKv, kD, kLoCols>(st + u * C::kPageBytes + C::kTileBytes, pb0, pb1,
+                                              pl0, pl1, ntok, lane, o);
                 }
             }
         }
@@ -838,6 +933,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
 
         // ---- piece finished: final output, or a partial for the reduce
         if (last) {
+            if constexpr (kLoCols) {
+                // add the low-part columns (lanes c + 2) to the high-part ones
+#pragma unroll
+                for (int i = 0; i < KS; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) o[i][j] += __shfl_xor_sync(0xffffffffu, o[i][j], 2);
+            }
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -851,15 +953,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
                 const int64_t orow = (static_cast<int64_t>(cc.seq) * p.num_heads + h0) * kD;
                 dstA = p.out + orow + static_cast<int64_t>(hA) * kD;
                 dstB = p.out + orow + static_cast<int64_t>(hB) * kD;
-                fA = piece_bad ? 0.f : 1.f / l0;
-                fB = piece_bad ? 0.f : 1.f / l1;
+                const float vs = (kInt8 ? vref : 1.f) * kPScaleInv;
+                fA = piece_bad ? 0.f : vs / l0;
+                fB = piece_bad ? 0.f : vs / l1;
             } else {
                 const int slotp = piece_has_a ? 0 : 1;
                 float *rec = p.partials +
                              (static_cast<int64_t>(w) * 2 + slotp) * p.rec_heads * (kD + 4);
                 dstA = rec + hA * (kD + 4) + 4;
                 dstB = rec + hB * (kD + 4) + 4;
-                fA = fB = 1.f;
+                fA = fB = (kInt8 ? vref : 1.f) * kPScaleInv;  // accumulators in V units
                 if (g == 0) {
                     if (hA < gh) {
                         dstA[-4] = m0;
@@ -1128,7 +1231,7 @@ struct OccCache {
     int per_sm = 0;
 };
 
-template <int kKv, int kD>
+template <int kKv, int kD, bool kLoCols>
 pkv_status launch(const DecodeCall &call, const Shape &sh)
 {
     using C = Cfg<kKv, kD>;
@@ -1136,7 +1239,7 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     if (!current_device_info(&di)) return PKV_ERR_CUDA;
     const size_t smem = C::smem_bytes(call.num_seqs);
     if (smem > di.max_smem_optin) return PKV_ERR_UNSUPPORTED;
-    auto kern = decode_kernel<kKv, kD>;
+    auto kern = decode_kernel<kKv, kD, kLoCols>;
     static OccCache occ[64];
     int per_sm = 0;
     int cap = 0;
@@ -1250,11 +1353,22 @@ pkv_status decode_entry(const DecodeCall &call, int kv)
     const size_t need = workspace_bytes_for(sh, call.head_dim);
     if (need > 0 && (!call.workspace || call.workspace_bytes < need)) return PKV_ERR_WORKSPACE;
     if (call.workspace && !aligned(call.workspace, 16)) return PKV_ERR_MISALIGNED;
-    if (kv == kKvF8)
-        return call.head_dim == 128 ? launch<kKvF8, 128>(call, sh) : launch<kKvF8, 64>(call, sh);
-    if (kv == kKvI8)
-        return call.head_dim == 128 ? launch<kKvI8, 128>(call, sh) : launch<kKvI8, 64>(call, sh);
-    return call.head_dim == 128 ? launch<kKvF16, 128>(call, sh) : launch<kKvF16, 64>(call, sh);
+    // groups of at most four query heads carry the low parts of the
+    // probabilities in the spare mma columns
+    const bool lo_cols = sh.group <= 4;
+    if (kv == kKvF8) {
+        if (call.head_dim == 128)
+            return lo_cols ? launch<kKvF8, 128, true>(call, sh) : launch<kKvF8, 128, false>(call, sh);
+        return lo_cols ? launch<kKvF8, 64, true>(call, sh) : launch<kKvF8, 64, false>(call, sh);
+    }
+    if (kv == kKvI8) {
+        if (call.head_dim == 128)
+            return lo_cols ? launch<kKvI8, 128, true>(call, sh) : launch<kKvI8, 128, false>(call, sh);
+        return lo_cols ? launch<kKvI8, 64, true>(call, sh) : launch<kKvI8, 64, false>(call, sh);
+    }
+    if (call.head_dim == 128)
+        return lo_cols ? launch<kKvF16, 128, true>(call, sh) : launch<kKvF16, 128, false>(call, sh);
+    return lo_cols ? launch<kKvF16, 64, true>(call, sh) : launch<kKvF16, 64, false>(call, sh);
 }
 
 }  // namespace
@@ -1394,5 +1508,20 @@ extern "C" __attribute__((visibility("default"))) unsigned int pkv_debug_flags(i
         if (cudaMemcpyToSymbol(pkv::g_debug_flags, &z, sizeof(z)) != cudaSuccess) return 0xffffffffu;
     }
     return v;
+}
+
+// Debug builds only: the limit of the decode kernel's waits for a stage, in
+// ns, on the current device (0: a wait gives up at once, as if its limit had
+// run out, while its copies are still in flight; the drain that follows a
+// timeout keeps its 1 s limit).  Negative restores the default of 1 s.  Synchronises with the
+// device; returns 0, or -1 if the CUDA runtime fails.
+extern "C" __attribute__((visibility("default"))) int pkv_debug_set_stage_wait_ns(long long ns)
+{
+    const unsigned long long v =
+        ns < 0 ? pkv::kWaitLimitNs : static_cast<unsigned long long>(ns);
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyToSymbol(pkv::g_debug_stage_wait_ns, &v, sizeof(v)) != cudaSuccess)
+        return -1;
+    return 0;
 }
 #endif

@@ -16,6 +16,22 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+
+// Recently encoded tensor maps.  A map depends only on the description it
+// was encoded from (base address, geometry, box, swizzle), so a call over
+// the same pools reuses it instead of encoding it again on the host.
+struct TmapEntry {
+    bool valid = false;
+    const void *base = nullptr;
+    int elem_bytes = 0, swizzle = 0;
+    uint64_t inner = 0, rows = 0;
+    uint32_t box_inner = 0, box_rows = 0;
+    CUtensorMap map;
+};
+constexpr int kTmapEntries = 16;
+TmapEntry g_tmaps[kTmapEntries];
+int g_tmap_next = 0;
+std::mutex g_tmap_mu;
 }  // namespace
 
 bool current_device_info(DeviceInfo *out)
@@ -54,6 +70,17 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
             g_encode = reinterpret_cast<EncodeTiledFn>(fn);
         }
     }
+    {
+        std::lock_guard<std::mutex> lock(g_tmap_mu);
+        for (const TmapEntry &e : g_tmaps) {
+            if (e.valid && e.base == base && e.elem_bytes == elem_bytes &&
+                e.swizzle == swizzle_bytes && e.inner == inner_elems && e.rows == rows &&
+                e.box_inner == box_inner && e.box_rows == box_rows) {
+                *map = e.map;
+                return true;
+            }
+        }
+    }
     const cuuint64_t dims[2] = {inner_elems, rows};
     const cuuint64_t strides[1] = {inner_elems * static_cast<uint64_t>(elem_bytes)};
     const cuuint32_t box[2] = {box_inner, box_rows};
@@ -66,7 +93,20 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
                                 CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    TmapEntry &e = g_tmaps[g_tmap_next];
+    g_tmap_next = (g_tmap_next + 1) % kTmapEntries;
+    e.base = base;
+    e.elem_bytes = elem_bytes;
+    e.swizzle = swizzle_bytes;
+    e.inner = inner_elems;
+    e.rows = rows;
+    e.box_inner = box_inner;
+    e.box_rows = box_rows;
+    e.map = *map;
+    e.valid = true;
+    return true;
 }
 
 }  // namespace pkv

@@ -99,8 +99,18 @@ def build(name: str, *, num_heads: int, num_kv_heads: int, head_dim: int,
           num_blocks: int, context_lens, seed: int,
           shared_prefix_blocks: int = 0, heavy_tail: bool = False,
           nan_padding: bool = True, block_size: int = BLOCK_SIZE,
-          max_blocks_per_seq: Optional[int] = None) -> DecodeWorkload:
-    """Lay out one synthetic decode batch.  See the module docstring."""
+          max_blocks_per_seq: Optional[int] = None, q_std: float = 1.0,
+          k_mult: float = 1.0, v_mult: float = 1.0,
+          v_hot_mult: float = 1.0) -> DecodeWorkload:
+    """Lay out one synthetic decode batch.  See the module docstring.
+
+    Magnitude options (all applied to the float32 draws before the fp16
+    cast; the defaults leave the draws unchanged): q ~ N(0, q_std^2); every K
+    value times ``k_mult``; every V value times ``v_mult``; and, when
+    ``v_hot_mult`` != 1, the V values of one seeded block of each sequence
+    (its own sub-stream) times ``v_hot_mult`` as well, so that the blocks of
+    one sequence hold V of very different magnitudes.
+    """
     ctx = np.asarray(context_lens, dtype=np.int32)
     n = int(ctx.size)
     nblk = [(int(c) + block_size - 1) // block_size for c in ctx]
@@ -129,9 +139,23 @@ def build(name: str, *, num_heads: int, num_kv_heads: int, head_dim: int,
         n_out = int(round(0.001 * k_used.size))
         pos = _rng(seed, 5).choice(k_used.size, size=n_out, replace=False)
         k_used.reshape(-1)[pos] *= 10.0
+    if k_mult != 1.0:
+        k_used *= np.float32(k_mult)
     k_pool[used] = k_used.astype(np.float16)
     del k_used
-    v_pool[used] = _normal_f16(_rng(seed, 2), used_shape)
+    v_used = _rng(seed, 2).standard_normal(used_shape, dtype=np.float32)
+    if v_mult != 1.0:
+        v_used *= np.float32(v_mult)
+    if v_hot_mult != 1.0:
+        rng_hot = _rng(seed, 9)
+        hot = set()
+        for s in range(n):
+            if nblk[s] > 0:
+                hot.add(int(tables[s, int(rng_hot.integers(0, nblk[s]))]))
+        rows = np.searchsorted(used, np.asarray(sorted(hot), dtype=np.int32))
+        v_used[rows] *= np.float32(v_hot_mult)
+    v_pool[used] = v_used.astype(np.float16)
+    del v_used
 
     if nan_padding:
         for s in range(n):
@@ -141,7 +165,10 @@ def build(name: str, *, num_heads: int, num_kv_heads: int, head_dim: int,
                 k_pool[last, :, c % block_size:, :] = np.nan
                 v_pool[last, :, c % block_size:, :] = np.nan
 
-    query = _normal_f16(_rng(seed, 0), (n, num_heads, head_dim))
+    q32 = _rng(seed, 0).standard_normal((n, num_heads, head_dim), dtype=np.float32)
+    if q_std != 1.0:
+        q32 *= np.float32(q_std)
+    query = q32.astype(np.float16)
     return DecodeWorkload(
         name=name, query=query, k_pool=k_pool, v_pool=v_pool,
         block_tables=tables, context_lens=ctx, num_heads=num_heads,
@@ -184,8 +211,9 @@ def make(name: str, nan_padding: bool = True) -> DecodeWorkload:
 def random_case(seed: int, *, num_seqs: int, num_heads: int, num_kv_heads: int,
                 head_dim: int, context_lens=None, max_ctx: int = 100,
                 extra_blocks: int = 3, nan_padding: bool = True,
-                block_size: int = BLOCK_SIZE) -> DecodeWorkload:
-    """A small seeded case for parity and edge-case tests."""
+                block_size: int = BLOCK_SIZE, **magnitudes) -> DecodeWorkload:
+    """A small seeded case for parity and edge-case tests (``magnitudes``:
+    the q_std / k_mult / v_mult / v_hot_mult options of ``build``)."""
     if context_lens is None:
         context_lens = _rng(seed, 4).integers(0, max_ctx, size=num_seqs, endpoint=True)
     ctx = np.asarray(context_lens, dtype=np.int32)
@@ -193,7 +221,7 @@ def random_case(seed: int, *, num_seqs: int, num_heads: int, num_kv_heads: int,
     return build(f"random_{seed}", num_heads=num_heads, num_kv_heads=num_kv_heads,
                  head_dim=head_dim, num_blocks=max(need + extra_blocks, 1),
                  context_lens=ctx, seed=seed, nan_padding=nan_padding,
-                 block_size=block_size)
+                 block_size=block_size, **magnitudes)
 
 
 def append_tokens(w: DecodeWorkload, seed: int):

@@ -57,9 +57,13 @@ def test_split_count_sweep(variant, workers):
     ref, _ = oracle_decode(w, variant, codes)
     assert st == 0
     assert_close(got, ref, f"workers={workers}")
-    # probabilities are rounded to fp16 relative to the running max, which
-    # depends on where each split starts, so splits agree to ~1e-4, not bitwise
-    assert np.max(np.abs(got - base)) < 5e-4
+    # every split merges to the same answer up to float rounding: the
+    # probabilities reach PV as fp32 values (an exact f16 high + low pair), so
+    # only the exp2 of differences taken against split-dependent running maxima
+    # and the order of fp32 additions differ
+    diff = float(np.max(np.abs(got - base)))
+    print(f"\nsplit {variant} workers={workers}: max |diff| vs automatic {diff:.3e}")
+    assert diff <= 1e-6
 
 
 @pytest.mark.parametrize("variant", VARIANTS)

@@ -4,9 +4,11 @@ pkv_paged_decode_int8_static_workspace serves callers that cannot allocate
 device memory themselves (their memory belongs to another allocator, or they
 cannot accept the device synchronisation an allocation may cause): its
 scratch is a fixed array inside the library.  Here it must give the same
-outputs as pkv_paged_decode_int8 with a caller-provided workspace, on two
-calls in a row (the second call reuses whatever the first left in the shared
-array), and refuse a call whose scratch would not fit.
+outputs as pkv_paged_decode_int8 with a caller-provided workspace, bit for
+bit (the same kernels with the same worker count run on the same inputs), on
+two calls in a row (the second call reuses whatever the first left in the
+shared array), match the oracle within the decode tolerance, and refuse a
+call whose scratch would not fit.
 
 This file is collected after every other test file, and its tests pass both
 in a fresh process and after the rest of the suite.
@@ -17,22 +19,16 @@ import torch
 
 import paged_kv_cache_234_gb300 as pkv
 import pkv_workloads as W
-from gpu_common import MAX_ABS, REL_L2, dev, ensure_built, oracle_codes
+from gpu_common import assert_close, dev, ensure_built, oracle_codes, oracle_decode
 
 pytestmark = pytest.mark.gpu
-
-
-def _close(got, ref):
-    err = np.abs(got - ref)
-    assert np.all(np.isfinite(got))
-    assert float(err.max()) <= MAX_ABS
-    assert float(np.linalg.norm(got - ref)) <= REL_L2 * float(np.linalg.norm(ref))
 
 
 def test_matches_the_workspace_entry_point_on_two_calls_in_a_row():
     ensure_built()
     w = W.random_case(91, num_seqs=16, num_heads=32, num_kv_heads=8, head_dim=128, max_ctx=1500)
-    kc, vc, ks, vs = (dev(x) for x in oracle_codes(w))
+    codes = oracle_codes(w)
+    kc, vc, ks, vs = (dev(x) for x in codes)
     n, hq, d = w.query.shape
     q, bt, cl = dev(w.query), dev(w.block_tables), dev(w.context_lens)
     mcl = w.max_context_len
@@ -43,7 +39,8 @@ def test_matches_the_workspace_entry_point_on_two_calls_in_a_row():
     ws = pkv.decode_workspace(n, hq, w.num_kv_heads, d, mcl)
     pkv.pkv_paged_decode_int8(ref, q, kc, vc, ks, vs, bt, cl, mcl, w.softmax_scale, ws)
     torch.cuda.synchronize()
-    ref_np = ref.cpu().numpy().astype(np.float64)
+    ref_np = ref.cpu().numpy()
+    want, _ = oracle_decode(w, "int8", codes)
 
     for _ in range(2):
         out = torch.full((n, hq, d), float("nan"), dtype=torch.float32, device="cuda")
@@ -52,7 +49,9 @@ def test_matches_the_workspace_entry_point_on_two_calls_in_a_row():
                                                    w.softmax_scale, status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        _close(out.cpu().numpy().astype(np.float64), ref_np)
+        got = out.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), ref_np.view(np.uint32))
+        assert_close(got.astype(np.float64), want, "static workspace")
 
 
 def test_refuses_a_call_whose_scratch_does_not_fit():
