@@ -85,8 +85,6 @@ struct DecodeArgs {
     const float *k_scales;
     const float *v_scales;
     float *partials;     // [num_workers * 2][rec_heads][head_dim + 4]
-    int4 *splits;        // [num_workers][2]: the split item whose first piece
-                         // the worker holds, if any (see SplitDesc)
     int32_t *dev_status;
     int num_seqs, num_heads, num_kv_heads;
     int group;           // query heads per kv head
@@ -248,9 +246,12 @@ __device__ __forceinline__ uint32_t swz(int t, int ch)
 // ------------------------------------------------------ per-sequence tables
 // ctxs[s]   = context length, or -1 if it is outside [0, ctx_cap]
 // prefix[s] = pages of all sequences before s (exclusive prefix sum)
+// Computed by a CTA of kNT threads from context_lens alone.
+template <int kNT = kThreads>
 __device__ void build_page_tables(const DecodeArgs &p, int32_t *prefix, int32_t *ctxs)
 {
-    __shared__ int32_t warp_sums[kWarps];
+    constexpr int kNW = kNT / 32;
+    __shared__ int32_t warp_sums[kNW];
     __shared__ int32_t carry;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
@@ -258,7 +259,7 @@ __device__ void build_page_tables(const DecodeArgs &p, int32_t *prefix, int32_t 
         prefix[0] = 0;
     }
     __syncthreads();
-    for (int base = 0; base < p.num_seqs; base += kThreads) {
+    for (int base = 0; base < p.num_seqs; base += kNT) {
         const int s = base + threadIdx.x;
         int np = 0;
         if (s < p.num_seqs) {
@@ -280,9 +281,19 @@ __device__ void build_page_tables(const DecodeArgs &p, int32_t *prefix, int32_t 
         const int incl = before + v;
         if (s < p.num_seqs) prefix[s + 1] = incl;
         __syncthreads();
-        if (threadIdx.x == kThreads - 1) carry = incl;
+        if (threadIdx.x == kNT - 1) carry = incl;
         __syncthreads();
     }
+}
+
+// floor(x * k / d) for x, k >= 0 and d > 0; a 32-bit division when the
+// operands fit (the usual case), else a 64-bit one.
+__device__ __forceinline__ int64_t muldiv(int64_t x, int64_t k, int64_t d)
+{
+    const uint64_t num = static_cast<uint64_t>(x) * static_cast<uint64_t>(k);
+    if (num <= 0xffffffffull && static_cast<uint64_t>(d) <= 0xffffffffull)
+        return static_cast<uint32_t>(num) / static_cast<uint32_t>(d);
+    return static_cast<int64_t>(num / static_cast<uint64_t>(d));
 }
 
 // Position of one page in the stream of all items' pages.
@@ -307,8 +318,14 @@ struct PageCursor {
         seq = lo;
         npages = prefix[PKV_IDX(lo + 1, p.num_seqs + 1)] - prefix[lo];
         const int64_t r = x - static_cast<int64_t>(p.items_per_seq) * prefix[lo];
-        item = static_cast<int>(r / npages);
-        page = static_cast<int>(r % npages);
+        if (r <= 0xffffffffll) {
+            const uint32_t r32 = static_cast<uint32_t>(r);
+            item = static_cast<int>(r32 / static_cast<uint32_t>(npages));
+            page = static_cast<int>(r32 - static_cast<uint32_t>(item) * static_cast<uint32_t>(npages));
+        } else {
+            item = static_cast<int>(r / npages);
+            page = static_cast<int>(r % npages);
+        }
         kvh = item / p.qgroups;
         qg = item - kvh * p.qgroups;
     }
@@ -368,19 +385,10 @@ __device__ __forceinline__ uint32_t i8pair_exact(uint32_t xw, uint32_t sel)
 // Which worker's page range holds stream page x (largest w with a_w <= x).
 __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t total, int workers)
 {
-    return ((x + 1) * workers - 1) / total;
-}
-
-// Per worker: the item split across workers whose first page lies in this
-// worker's range, if any.  Word 0: bit 0 valid, bit 1 the record slot of
-// this worker, bit 2 "every worker has pages"; then the last worker holding
-// a piece of the item, the sequence, the item, and the stream length.
-__device__ __forceinline__ void write_split(const DecodeArgs &p, int w, bool valid, int slot,
-                                            int64_t last_worker, int seq, int item, int64_t total)
-{
-    const int flags = (valid ? 1 : 0) | (slot << 1) | (total >= p.num_workers ? 4 : 0);
-    p.splits[2 * w] = make_int4(flags, static_cast<int>(last_worker), seq, item);
-    p.splits[2 * w + 1] = make_int4(static_cast<int>(total), 0, 0, 0);
+    const uint64_t num = static_cast<uint64_t>(x + 1) * static_cast<uint64_t>(workers) - 1;
+    if (num <= 0xffffffffull && static_cast<uint64_t>(total) <= 0xffffffffull)
+        return static_cast<uint32_t>(num) / static_cast<uint32_t>(total);
+    return static_cast<int64_t>(num / static_cast<uint64_t>(total));
 }
 
 // S^T fragment (rows: tokens g, g+8; cols: heads 2c, 2c+1) of one page.
@@ -564,6 +572,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
         ptx::prefetch_tmap(&tmk);
         ptx::prefetch_tmap(&tmv);
     }
+    // This warp's stage barriers, set up before anything else (shared memory
+    // only) so that the fence making them visible to the copy engine is done
+    // by the time the first copies are issued.
+    const uint32_t bar0 = ptx::smem_addr(smem + C::kBarOffset) + warp * S * 8;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) ptx::mbar_init(PKV_SMEM(bar0 + 8 * s, 8, 8), kInt8 ? 2 : 1);
+        ptx::fence_mbar_init();
+    }
+    __syncwarp();
     // Launched as a programmatic dependent of the previous kernel on the
     // stream: wait until its writes are visible before reading any input.
     ptx::griddep_wait();
@@ -584,22 +601,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
 
     const int w = blockIdx.x * kWarps + warp;
     if (w >= p.num_workers) return;
-    if (lane == 0) write_split(p, w, false, 0, 0, 0, 0, total);  // no split item yet
     if (total == 0) return;
-    const int64_t a = w * total / p.num_workers;
-    const int64_t b = (w + 1) * total / p.num_workers;
+    const int64_t a = muldiv(w, total, p.num_workers);
+    const int64_t b = muldiv(w + 1, total, p.num_workers);
     if (a >= b) return;
     const int n = static_cast<int>(b - a);  // pages of this worker
 
     const uint32_t stage0 = ptx::smem_addr(smem) + warp * S * C::kStageBytes;
     uint8_t *hdr_base = smem + C::kHdrOffset + warp * S * C::kHdrBytes;
     const uint32_t hdr0 = ptx::smem_addr(hdr_base);
-    const uint32_t bar0 = ptx::smem_addr(smem + C::kBarOffset) + warp * S * 8;
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) ptx::mbar_init(PKV_SMEM(bar0 + 8 * s, 8, 8), kInt8 ? 2 : 1);
-        ptx::fence_mbar_init();
-    }
-    __syncwarp();
     const uint64_t policy = ptx::policy_evict_first();
     const int64_t mb = p.max_blocks_per_seq;
     const uint64_t stage_wait_ns = PKV_STAGE_WAIT_NS;
@@ -978,14 +988,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
 #pragma unroll
                 for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             }
-            if (!whole && piece_first_page == 0 && lane == 0) {
-                // this piece starts an item that later workers continue
-                const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[PKV_IDX(cc.seq, p.num_seqs)] +
-                                   static_cast<int64_t>(cc.item) * cc.npages;
-                write_split(p, w, true, piece_has_a ? 0 : 1,
-                            worker_of(s0 + cc.npages - 1, total, p.num_workers), cc.seq, cc.item,
-                            total);
-            }
             if constexpr (!kInt8) {
 #pragma unroll
                 for (int i = 0; i < KS; ++i) {
@@ -1018,129 +1020,155 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     }
 }
 
-// Split-context reduce: one warp per (worker, query head).  A worker whose
-// range holds the first piece of a split item merges that item:
+// Split-context reduce.  Tasks are (item, query head); a warp takes tasks
+// gw, gw + warps, ... and merges those whose item is split across workers:
 //   out = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w,  M = max_w m_w
-// over the pieces of workers first .. last.  A piece flagged bad (l < 0)
-// zeroes the item.  With up to eight pieces (the usual case) every load of
-// every piece is issued at once; otherwise lanes read the (m, l) of up to 32
-// pieces at a time, then the accumulators four pieces per batch.  Lanes run
-// across head_dim; pieces are combined in a fixed order.
+// over the pieces of the workers holding the item's first .. last page.  A
+// piece flagged bad (l < 0) zeroes the item.  Which items are split, which
+// workers hold their pieces and where those records are depend only on the
+// partition of the page stream, i.e. on context_lens, an input of the call:
+// all of it is worked out before the kernel waits for the decode grid, so
+// that after the wait only the records are read (every load of up to eight
+// pieces at once; beyond that the (m, l) of 32 pieces per round, one lane per
+// piece, then the accumulators four pieces per batch).  Lanes run across
+// head_dim; pieces are combined in a fixed order.
+constexpr int kRedThreads = 128;
+constexpr int kRedCtasPerSm = 4;  // a grid that fits in one wave once the decode is gone
+
 template <int kD>
-__global__ void __launch_bounds__(kThreads) reduce_kernel(const DecodeArgs p)
+__global__ void __launch_bounds__(kRedThreads) reduce_kernel(const DecodeArgs p)
 {
-    ptx::griddep_wait();  // the decode grid's records are complete and visible
+    extern __shared__ __align__(16) uint8_t rsmem[];
+    int32_t *prefix = reinterpret_cast<int32_t *>(rsmem);
+    int32_t *ctxs = prefix + p.num_seqs + 1;
+    build_page_tables<kRedThreads>(p, prefix, ctxs);
     const int lane = threadIdx.x & 31;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    const int wf = static_cast<int>(gw / p.rec_heads);
-    const int h = static_cast<int>(gw - static_cast<int64_t>(wf) * p.rec_heads);
-    if (wf >= p.num_workers) return;
-    const int4 d0 = __ldcg(p.splits + 2 * wf);
-    if (!(d0.x & 1)) return;
-    const int seq = d0.z, item = d0.w;
-    const int kvh = item / p.qgroups, qg = item - kvh * p.qgroups;
-    const int h0 = kvh * p.group + qg * kItemHeads;
-    const int gh = min(kItemHeads, p.group - qg * kItemHeads);
-    if (h >= gh) return;
-    const int nw = d0.y - wf + 1;
-    const int slot0 = (d0.x >> 1) & 1;
-    const bool dense = (d0.x & 4) != 0;
-    const int64_t total = dense ? 0 : __ldcg(p.splits + 2 * wf + 1).x;
     const int W = p.num_workers;
+    const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
+    const int64_t per_seq = static_cast<int64_t>(p.items_per_seq) * p.rec_heads;
+    const int64_t ntasks = per_seq * p.num_seqs;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kRedThreads / 32);
+    bool waited = false;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * (kRedThreads / 32) + (threadIdx.x >> 5);
+         t < ntasks; t += nwarps) {
+        const int seq = static_cast<int>(t / per_seq);
+        const int rem = static_cast<int>(t - seq * per_seq);
+        const int item = rem / p.rec_heads;
+        const int h = rem - item * p.rec_heads;
+        const int kvh = item / p.qgroups, qg = item - kvh * p.qgroups;
+        const int gh = min(kItemHeads, p.group - qg * kItemHeads);
+        const int npages = prefix[seq + 1] - prefix[seq];
+        if (h >= gh || npages == 0) continue;
+        const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[seq] +
+                           static_cast<int64_t>(item) * npages;  // the item's first page
+        const int64_t last = s0 + npages - 1;
+        const int wf = static_cast<int>(worker_of(s0, total, W));
+        const int nw = static_cast<int>(worker_of(last, total, W)) - wf + 1;
+        if (nw == 1) continue;  // whole inside one worker: finished by the decode
+        const int slot0 = s0 == muldiv(wf, total, W) ? 0 : 1;
 
-    // the record of piece j of this item (null: a worker with no pages)
-    auto rec_of = [&](int j) -> const float * {
-        const int64_t w = wf + j;
-        if (!dense && j > 0 && w * total / W == (w + 1) * total / W) return nullptr;
-        const int slot = j == 0 ? slot0 : 0;
-        return p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
-    };
+        // the record of piece j of this item (null: a worker with no pages)
+        auto rec_of = [&](int j) -> const float * {
+            const int64_t w = wf + j;
+            if (j > 0 && muldiv(w, total, W) == muldiv(w + 1, total, W)) return nullptr;
+            const int slot = j == 0 ? slot0 : 0;
+            return p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
+        };
+        constexpr int kFast = 8;  // pieces whose loads are all issued at once
+        const float *rp[kFast];
+#pragma unroll
+        for (int j = 0; j < kFast; ++j) rp[j] = j < nw ? rec_of(j) : nullptr;
+        if (!waited) {
+            ptx::griddep_wait();  // the decode grid's records are complete and visible
+            waited = true;
+        }
 
-    float acc[kD / 32];
+        float acc[kD / 32];
 #pragma unroll
-    for (int i = 0; i < kD / 32; ++i) acc[i] = 0.f;
-    float L = 0.f;
-    bool bad = false;
-    constexpr int kFast = 8;  // pieces whose loads are all issued at once
-    if (nw <= kFast) {
-        // common case: every load of every piece issued at once
-        float m[kFast], l[kFast], v[kFast][kD / 32];
+        for (int i = 0; i < kD / 32; ++i) acc[i] = 0.f;
+        float L = 0.f;
+        bool bad = false;
+        if (nw <= kFast) {
+            float m[kFast], l[kFast], v[kFast][kD / 32];
 #pragma unroll
-        for (int j = 0; j < kFast; ++j) {
-            const float *r = j < nw ? rec_of(j) : nullptr;
-            if (r) {
-                m[j] = __ldcg(r);
-                l[j] = __ldcg(r + 1);
+            for (int j = 0; j < kFast; ++j) {
+                const float *r = rp[j];
+                if (r) {
+                    m[j] = __ldcg(r);
+                    l[j] = __ldcg(r + 1);
 #pragma unroll
-                for (int i = 0; i < kD / 32; ++i) v[j][i] = __ldcg(r + 4 + lane + 32 * i);
-            } else {
-                m[j] = -INFINITY;
-                l[j] = 0.f;
+                    for (int i = 0; i < kD / 32; ++i) v[j][i] = __ldcg(r + 4 + lane + 32 * i);
+                } else {
+                    m[j] = -INFINITY;
+                    l[j] = 0.f;
 #pragma unroll
-                for (int i = 0; i < kD / 32; ++i) v[j][i] = 0.f;
-            }
-        }
-        float M = m[0];
-#pragma unroll
-        for (int j = 1; j < kFast; ++j) M = fmaxf(M, m[j]);
-#pragma unroll
-        for (int j = 0; j < kFast; ++j) {
-            const float f = m[j] == -INFINITY ? 0.f : ptx::ex2(m[j] - M);
-            bad |= l[j] < 0.f;
-            L += f * l[j];
-#pragma unroll
-            for (int i = 0; i < kD / 32; ++i) acc[i] += f * v[j][i];
-        }
-    } else {
-        float M = -INFINITY;
-        for (int base = 0; base < nw; base += 32) {
-            const float *r = base + lane < nw ? rec_of(base + lane) : nullptr;
-            if (r) {
-                M = fmaxf(M, __ldcg(r));
-                bad |= __ldcg(r + 1) < 0.f;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        bad = __any_sync(0xffffffffu, bad);
-        for (int base = 0; base < nw; base += 32) {
-            const float *mine = base + lane < nw ? rec_of(base + lane) : nullptr;
-            const float f_lane = mine ? ptx::ex2(__ldcg(mine) - M) : 0.f;
-            float Lp = mine ? f_lane * __ldcg(mine + 1) : 0.f;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, off);
-            L += Lp;
-            const uint64_t mbits = reinterpret_cast<uint64_t>(mine);
-            const uint32_t mlo = static_cast<uint32_t>(mbits);
-            const uint32_t mhi = static_cast<uint32_t>(mbits >> 32);
-            const int cnt = min(32, nw - base);
-            for (int j0 = 0; j0 < cnt; j0 += 4) {
-                float v[4][kD / 32], f[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int src = min(j0 + u, 31);
-                    const uint64_t bits =
-                        (static_cast<uint64_t>(__shfl_sync(0xffffffffu, mhi, src)) << 32) |
-                        __shfl_sync(0xffffffffu, mlo, src);
-                    f[u] = __shfl_sync(0xffffffffu, f_lane, src);
-                    const float *r = reinterpret_cast<const float *>(bits);
-                    const bool use = j0 + u < cnt && r != nullptr;
-                    if (!use) f[u] = 0.f;
-#pragma unroll
-                    for (int i = 0; i < kD / 32; ++i)
-                        v[u][i] = use ? __ldcg(r + 4 + lane + 32 * i) : 0.f;
+                    for (int i = 0; i < kD / 32; ++i) v[j][i] = 0.f;
                 }
+            }
+            float M = m[0];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+            for (int j = 1; j < kFast; ++j) M = fmaxf(M, m[j]);
 #pragma unroll
-                    for (int i = 0; i < kD / 32; ++i) acc[i] += f[u] * v[u][i];
+            for (int j = 0; j < kFast; ++j) {
+                const float f = m[j] == -INFINITY ? 0.f : ptx::ex2(m[j] - M);
+                bad |= l[j] < 0.f;
+                L += f * l[j];
+#pragma unroll
+                for (int i = 0; i < kD / 32; ++i) acc[i] += f * v[j][i];
+            }
+        } else {
+            float M = -INFINITY;
+            for (int base = 0; base < nw; base += 32) {
+                const float *r = base + lane < nw ? rec_of(base + lane) : nullptr;
+                if (r) {
+                    M = fmaxf(M, __ldcg(r));
+                    bad |= __ldcg(r + 1) < 0.f;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            bad = __any_sync(0xffffffffu, bad);
+            for (int base = 0; base < nw; base += 32) {
+                const float *mine = base + lane < nw ? rec_of(base + lane) : nullptr;
+                const float f_lane = mine ? ptx::ex2(__ldcg(mine) - M) : 0.f;
+                float Lp = mine ? f_lane * __ldcg(mine + 1) : 0.f;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, off);
+                L += Lp;
+                const uint64_t mbits = reinterpret_cast<uint64_t>(mine);
+                const uint32_t mlo = static_cast<uint32_t>(mbits);
+                const uint32_t mhi = static_cast<uint32_t>(mbits >> 32);
+                const int cnt = min(32, nw - base);
+                for (int j0 = 0; j0 < cnt; j0 += 4) {
+                    float v[4][kD / 32], f[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int src = min(j0 + u, 31);
+                        const uint64_t bits =
+                            (static_cast<uint64_t>(__shfl_sync(0xffffffffu, mhi, src)) << 32) |
+                            __shfl_sync(0xffffffffu, mlo, src);
+                        f[u] = __shfl_sync(0xffffffffu, f_lane, src);
+                        const float *r = reinterpret_cast<const float *>(bits);
+                        const bool use = j0 + u < cnt && r != nullptr;
+                        if (!use) f[u] = 0.f;
+#pragma unroll
+                        for (int i = 0; i < kD / 32; ++i)
+                            v[u][i] = use ? __ldcg(r + 4 + lane + 32 * i) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int i = 0; i < kD / 32; ++i) acc[i] += f[u] * v[u][i];
+                }
             }
         }
-    }
-    float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
-    const float inv = bad ? 0.f : 1.f / L;
+        const int h0 = kvh * p.group + qg * kItemHeads;
+        float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
+        const float inv = bad ? 0.f : 1.f / L;
 #pragma unroll
-    for (int i = 0; i < kD / 32; ++i) dst[lane + 32 * i] = bad ? 0.f : acc[i] * inv;
+        for (int i = 0; i < kD / 32; ++i) dst[lane + 32 * i] = bad ? 0.f : acc[i] * inv;
+    }
 }
 
 // Launch with programmatic stream serialisation: the kernel may begin while
@@ -1211,18 +1239,12 @@ pkv_status check_shape(int num_seqs, int num_heads, int num_kv_heads, int head_d
     return PKV_OK;
 }
 
-// workspace: the partial records of up to min(4096, pages) workers, then
-// two int4 split descriptors per worker
-size_t partial_bytes_for(const Shape &sh, int head_dim)
-{
-    const int64_t workers = sh.max_pages < kMaxWorkers ? sh.max_pages : kMaxWorkers;
-    return static_cast<size_t>(workers) * 2 * sh.rec_heads * (head_dim + 4) * sizeof(float);
-}
-
+// workspace: two partial records (first and last piece) for each of up to
+// min(4096, pages) workers
 size_t workspace_bytes_for(const Shape &sh, int head_dim)
 {
     const int64_t workers = sh.max_pages < kMaxWorkers ? sh.max_pages : kMaxWorkers;
-    return partial_bytes_for(sh, head_dim) + static_cast<size_t>(workers) * 2 * sizeof(int4);
+    return static_cast<size_t>(workers) * 2 * sh.rec_heads * (head_dim + 4) * sizeof(float);
 }
 
 struct OccCache {
@@ -1290,8 +1312,6 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     args.k_scales = call.k_scales;
     args.v_scales = call.v_scales;
     args.partials = static_cast<float *>(call.workspace);
-    args.splits = reinterpret_cast<int4 *>(static_cast<uint8_t *>(call.workspace) +
-                                           partial_bytes_for(sh, call.head_dim));
     args.dev_status = call.dev_status;
     args.num_seqs = call.num_seqs;
     args.num_heads = call.num_heads;
@@ -1313,10 +1333,28 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
         return PKV_ERR_CUDA;
     }
     if (workers > 1) {
-        const int64_t warps = workers * sh.rec_heads;
-        const int64_t rgrid = (warps + kWarps - 1) / kWarps;
+        constexpr int kRedWarps = kRedThreads / 32;
+        const int64_t tasks =
+            static_cast<int64_t>(call.num_seqs) * sh.items_per_seq * sh.rec_heads;
+        int64_t rgrid = (tasks + kRedWarps - 1) / kRedWarps;
+        if (rgrid > static_cast<int64_t>(kRedCtasPerSm) * di.num_sms)
+            rgrid = static_cast<int64_t>(kRedCtasPerSm) * di.num_sms;
+        const size_t rsmem = static_cast<size_t>(2 * call.num_seqs + 1) * sizeof(int32_t);
         auto rk = reduce_kernel<kD>;
-        if (launch_pdl(rk, static_cast<unsigned>(rgrid), kThreads, 0, st, args) != cudaSuccess) {
+        {
+            // the per-sequence tables of the largest batch, once per device
+            static int red_ready[64] = {};
+            std::lock_guard<std::mutex> lock(g_cfg_mu);
+            if (!red_ready[di.device & 63]) {
+                if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>((2 * kMaxSeqs + 1) * sizeof(int32_t))) !=
+                    cudaSuccess)
+                    return PKV_ERR_CUDA;
+                red_ready[di.device & 63] = 1;
+            }
+        }
+        if (launch_pdl(rk, static_cast<unsigned>(rgrid), kRedThreads, rsmem, st, args) !=
+            cudaSuccess) {
             cudaGetLastError();
             return PKV_ERR_CUDA;
         }

@@ -94,6 +94,12 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// Prefetch the 128-byte line holding a global address into L2 (a hint).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

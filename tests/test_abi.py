@@ -48,11 +48,10 @@ def test_status_strings(L):
 
 
 def test_workspace_size_arithmetic(L):
-    # per worker: two partial records of min(8, group) heads x (d + 4) floats
-    # and two 16-byte split descriptors; at most 4096 workers and never more
-    # than the pages.
+    # per worker: two partial records of min(8, group) heads x (d + 4) floats;
+    # at most 4096 workers and never more than the pages.
     def expect(workers, heads, d):
-        return workers * (2 * heads * (d + 4) * 4 + 32)
+        return workers * 2 * heads * (d + 4) * 4
     assert pkv.pkv_decode_workspace_size(64, 32, 8, 128, 2048) == expect(4096, 4, 128)
     assert pkv.pkv_decode_workspace_size(2, 8, 2, 64, 37) == expect(2 * 2 * 3, 4, 64)
     assert pkv.pkv_decode_workspace_size(8, 8, 8, 128, 512) == expect(2048, 1, 128)

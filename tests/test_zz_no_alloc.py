@@ -57,7 +57,7 @@ def test_matches_the_workspace_entry_point_on_two_calls_in_a_row():
 def test_refuses_a_call_whose_scratch_does_not_fit():
     ensure_built()
     # 8 query heads per kv head, head_dim 128 and 4096 pages in flight need
-    # 4096 workers x (2 x 8 x 132 x 4 + 32) bytes: more than the fixed array
+    # 4096 workers x 2 x 8 x 132 x 4 bytes: more than the fixed array
     n, hq, hkv, d, mcl = 1, 64, 8, 128, 8192
     assert pkv.pkv_decode_workspace_size(n, hq, hkv, d, mcl) > pkv.PKV_STATIC_WORKSPACE_BYTES
     q = torch.zeros((n, hq, d), dtype=torch.float16, device="cuda")
