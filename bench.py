@@ -433,7 +433,8 @@ def run_report(args):
             bu = decode_bytes(uniq_ctx, hkv, d, eb, sc)
             t50, t90 = statistics.median(ts), float(np.percentile(ts, 90))
             rec = {"config": name, "variant": variant, "p50_us": 1e6 * t50,
-                   "p90_us": 1e6 * t90, "kv_bytes": b, "unique_kv_bytes": bu,
+                   "p90_us": 1e6 * t90, "mean_us": 1e6 * statistics.mean(ts),
+                   "kv_bytes": b, "unique_kv_bytes": bu,
                    "GB/s": b / t50 / 1e9, "frac_of_peak": b / t50 / 1e9 / peak,
                    "seq_steps_per_s": n / t50}
             if variant == "int8" and cpu is not None:

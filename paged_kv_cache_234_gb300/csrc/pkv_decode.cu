@@ -70,6 +70,7 @@ constexpr int kMaxWorkersPerItem = 4;  // measured on GB300: 8 x 512, 32 x 1024 
                                        // shape batches run 10-30 % faster than with one
                                        // worker per resident warp
 constexpr int kMaxSeqs = 8192;         // per-sequence tables live in shared memory
+constexpr int kMaxCluster = 8;         // CTAs per cluster in the one-item-per-cluster mode
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
 constexpr float kPScale = 32768.f;     // probabilities enter PV as 2^15 p (see the main loop)
 constexpr float kPScaleInv = 1.f / 32768.f;
@@ -95,6 +96,7 @@ struct DecodeArgs {
     int num_blocks;
     int ctx_cap;         // largest valid context length
     int num_workers;
+    int clust;           // 0: persistent workers; else one item per cluster of this many CTAs
     float scale_log2;    // softmax_scale * log2(e)
 };
 
@@ -226,6 +228,15 @@ struct Cfg {
     static size_t smem_bytes(int num_seqs)
     {
         return 1024 + kTabOffset + static_cast<size_t>(2 * num_seqs + 1) * sizeof(int32_t);
+    }
+    // One item per cluster: the records pushed to this CTA, after the tables.
+    __host__ __device__ static size_t crec_offset(int num_seqs)
+    {
+        return (kTabOffset + static_cast<size_t>(2 * num_seqs + 1) * sizeof(int32_t) + 15) & ~size_t(15);
+    }
+    static size_t crec_bytes(int warps, int heads_per_cta)
+    {
+        return static_cast<size_t>(warps) * heads_per_cta * (kD + 4) * sizeof(float);
     }
 };
 
@@ -548,7 +559,9 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
 // probability to PV and lanes holding columns 4-7 the low part, and the two
 // column halves of O^T are added when a piece ends.  Larger groups use all
 // eight columns and a second PV mma for the low parts.
-template <int kKv, int kD, bool kLoCols>
+// kClust: one item per thread-block cluster of p.clust CTAs (small batches);
+// otherwise persistent workers over the whole page stream.
+template <int kKv, int kD, bool kLoCols, bool kClust>
 __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv)
@@ -587,31 +600,78 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     // The next kernel on the stream may begin its own launch now; it waits
     // for this grid's completion before reading anything this grid writes.
     ptx::griddep_launch_dependents();
-    build_page_tables(p, prefix, ctxs);
-    const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
+    const int64_t mb = p.max_blocks_per_seq;
 
-    // Sequences with no pages: zero output (bad lengths are also reported).
-    for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x) {
-        if (prefix[s + 1] != prefix[s]) continue;
-        if (ctxs[s] < 0 && threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, PKV_DEV_BAD_CTX);
-        float4 *o = reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(s) * p.num_heads * kD);
-        for (int i = threadIdx.x; i < p.num_heads * kD / 4; i += kThreads)
-            o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    int n = 0;       // pages of this worker
+    PageCursor ci;   // its first page
+    int w = 0;       // persistent workers: the worker's index
+    // One item per cluster: the item's pages of the longest possible context
+    // (cP) are split evenly over the cluster's cW warps, this warp being cw;
+    // the item's actual pages are cnp, its sequence's context length cctx.
+    int cP = 0, cW = 0, cw = 0, cnp = 0, cctx = 0;
+    int32_t pre_blk = 0;  // block id of page (first page + lane), cluster mode
+    // cluster mode: the record of head h of this warp's piece, in the shared
+    // memory of the CTA that merges head h (rank h mod clust), slot
+    // (h / clust) * cW + cw; the layout of a partial record (m, l, -, -, acc)
+    float *crec = reinterpret_cast<float *>(smem + C::crec_offset(p.num_seqs));
+    auto crec_of = [&](int h) -> float * {
+        const int slot = (h / p.clust) * cW + cw;
+        return static_cast<float *>(ptx::map_generic(crec + slot * (kD + 4), h % p.clust));
+    };
+    if constexpr (kClust) {
+        const int r = static_cast<int>(ptx::cluster_ctarank());
+        const int gi = blockIdx.x / p.clust;  // the cluster's item
+        const int seq = gi / p.items_per_seq, item = gi - seq * p.items_per_seq;
+        cP = (p.ctx_cap + kPage - 1) / kPage;
+        cW = p.clust * kWarps;
+        cw = r * kWarps + warp;
+        const int lo = static_cast<int>(static_cast<int64_t>(cw) * cP / cW);
+        const int hi = static_cast<int>(static_cast<int64_t>(cw + 1) * cP / cW);
+        // the block ids of this warp's first stages (pages below cP are in
+        // the table row) and the context length, in one round trip
+        if (lane < S * PPS && lo + lane < hi)
+            pre_blk = __ldg(PKV_TABLE_AT(p, seq, lo, lane, mb));
+        const int cx = __ldg(p.context_lens + seq);
+        const bool ok = cx >= 0 && cx <= p.ctx_cap;
+        cctx = ok ? cx : -1;
+        cnp = ok ? (cx + kPage - 1) / kPage : 0;
+        n = max(0, min(hi, cnp) - lo);
+        ci.seq = seq;
+        ci.item = item;
+        ci.kvh = item / p.qgroups;
+        ci.qg = item - ci.kvh * p.qgroups;
+        ci.page = lo;
+        ci.npages = cnp;
+        if (!ok && cw == 0 && lane == 0 && p.dev_status) atomicOr(p.dev_status, PKV_DEV_BAD_CTX);
+    } else {
+        build_page_tables(p, prefix, ctxs);
+        const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
+
+        // Sequences with no pages: zero output (bad lengths are also reported).
+        for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x) {
+            if (prefix[s + 1] != prefix[s]) continue;
+            if (ctxs[s] < 0 && threadIdx.x == 0 && p.dev_status)
+                atomicOr(p.dev_status, PKV_DEV_BAD_CTX);
+            float4 *o =
+                reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(s) * p.num_heads * kD);
+            for (int i = threadIdx.x; i < p.num_heads * kD / 4; i += kThreads)
+                o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+
+        w = blockIdx.x * kWarps + warp;
+        if (w >= p.num_workers) return;
+        if (total == 0) return;
+        const int64_t a = muldiv(w, total, p.num_workers);
+        const int64_t b = muldiv(w + 1, total, p.num_workers);
+        if (a >= b) return;
+        n = static_cast<int>(b - a);
+        ci.seek(p, prefix, a);
     }
-
-    const int w = blockIdx.x * kWarps + warp;
-    if (w >= p.num_workers) return;
-    if (total == 0) return;
-    const int64_t a = muldiv(w, total, p.num_workers);
-    const int64_t b = muldiv(w + 1, total, p.num_workers);
-    if (a >= b) return;
-    const int n = static_cast<int>(b - a);  // pages of this worker
 
     const uint32_t stage0 = ptx::smem_addr(smem) + warp * S * C::kStageBytes;
     uint8_t *hdr_base = smem + C::kHdrOffset + warp * S * C::kHdrBytes;
     const uint32_t hdr0 = ptx::smem_addr(hdr_base);
     const uint64_t policy = ptx::policy_evict_first();
-    const int64_t mb = p.max_blocks_per_seq;
     const uint64_t stage_wait_ns = PKV_STAGE_WAIT_NS;
 
     // Lane 0: start the copies of the `cnt` pages of one stage; blk[u] are
@@ -655,8 +715,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     };
 
     // ---- prologue: block ids of the first stages (one lane per page), issue
-    PageCursor ci;
-    ci.seek(p, prefix, a);
     PageCursor cc = ci;
     int ipos = 0;          // pages issued so far
     uint32_t issued = 0;   // stages issued so far
@@ -672,7 +730,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             if (j == my_stage) {
                 mycnt = cnt;
                 mykvh = cj.kvh;
-                if (my_u < cnt) myblk = __ldg(PKV_TABLE_AT(p, cj.seq, cj.page, my_u, mb));
+                // cluster mode: one item, pages in order, ids loaded above
+                if (my_u < cnt)
+                    myblk = kClust ? pre_blk : __ldg(PKV_TABLE_AT(p, cj.seq, cj.page, my_u, mb));
             }
             cj.advance(p, prefix, cnt);
             pos += cnt;
@@ -711,6 +771,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     int piece_first_page = 0;
     int piece_pages = 0;
 
+    bool timed_out = false;
     int pos = 0;
     for (uint32_t k = 0; pos < n; ++k) {
         const int slot = static_cast<int>(k % S);
@@ -787,7 +848,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             for (uint32_t r = k; r < issued; ++r)
                 ptx::mbar_wait_bounded(PKV_SMEM(bar0 + 8 * (r % S), 8, 8), (r / S) & 1u,
                                        kWaitLimitNs);
-            return;
+            if constexpr (!kClust) return;
+            timed_out = true;  // the cluster's merge still needs this warp
+            break;
         }
 
         const int32_t *hb = reinterpret_cast<const int32_t *>(hdr_base + slot * C::kHdrBytes);
@@ -802,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
         }
         if (any_good) {
             const uint32_t st = stage0 + slot * C::kStageBytes;
-            const int ctx = ctxs[PKV_IDX(cc.seq, p.num_seqs)];
+            const int ctx = kClust ? cctx : ctxs[PKV_IDX(cc.seq, p.num_seqs)];
             // ---- scores of the stage's pages, base-2 logits
             float x[PPS][4];
 #pragma unroll
@@ -955,7 +1018,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
                 l0 += __shfl_xor_sync(0xffffffffu, l0, off);
                 l1 += __shfl_xor_sync(0xffffffffu, l1, off);
             }
-            const bool whole = piece_first_page == 0 && cc.page + cnt == cc.npages;
+            const bool whole =
+                !kClust && piece_first_page == 0 && cc.page + cnt == cc.npages;
             const int hA = 2 * c, hB = 2 * c + 1;
             float *dstA, *dstB;
             float fA, fB;
@@ -967,11 +1031,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
                 fA = piece_bad ? 0.f : vs / l0;
                 fB = piece_bad ? 0.f : vs / l1;
             } else {
-                const int slotp = piece_has_a ? 0 : 1;
-                float *rec = p.partials +
-                             (static_cast<int64_t>(w) * 2 + slotp) * p.rec_heads * (kD + 4);
-                dstA = rec + hA * (kD + 4) + 4;
-                dstB = rec + hB * (kD + 4) + 4;
+                if constexpr (kClust) {
+                    // pushed to the shared memory of the CTAs merging hA, hB
+                    dstA = hA < gh ? crec_of(hA) + 4 : nullptr;
+                    dstB = hB < gh ? crec_of(hB) + 4 : nullptr;
+                } else {
+                    const int slotp = piece_has_a ? 0 : 1;
+                    float *rec = p.partials + (static_cast<int64_t>(w) * 2 + slotp) *
+                                                  p.rec_heads * (kD + 4);
+                    dstA = rec + hA * (kD + 4) + 4;
+                    dstB = rec + hB * (kD + 4) + 4;
+                }
                 fA = fB = (kInt8 ? vref : 1.f) * kPScaleInv;  // accumulators in V units
                 if (g == 0) {
                     if (hA < gh) {
@@ -1018,6 +1088,67 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
         cc.advance(p, prefix, cnt);
         pos += cnt;
     }
+    if constexpr (!kClust) return;
+    else {
+
+    // ---- one item per cluster: merge the cluster's pieces of the item
+    // Every warp with pages has pushed its (m, l, acc) record of each head h
+    // into the shared memory of CTA h mod clust (one that timed out pushes a
+    // bad mark).  After one cluster barrier every CTA merges its heads from
+    // its own shared memory, in piece order:
+    //   out = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j,  M = max_j m_j
+    // and nothing reads another CTA's memory after the barrier.
+    const int gi = blockIdx.x / p.clust;
+    const int seq = gi / p.items_per_seq, item = gi - seq * p.items_per_seq;
+    const int kvh = item / p.qgroups, qg = item - kvh * p.qgroups;
+    const int gh = min(kItemHeads, p.group - qg * kItemHeads);
+    const int h0 = kvh * p.group + qg * kItemHeads;
+    if (timed_out && lane < gh) crec_of(lane)[1] = -1.f;
+    __syncwarp();
+    ptx::cluster_sync();
+    const int rank = static_cast<int>(ptx::cluster_ctarank());
+    constexpr int kChunks = kD / 32;
+    const int my_heads = gh > rank ? (gh - rank + p.clust - 1) / p.clust : 0;
+    for (int t = warp; t < my_heads * kChunks; t += kWarps) {
+        const int hl = t / kChunks, ch = t - hl * kChunks;
+        const int h = rank + hl * p.clust;
+        const float *rb = crec + hl * cW * (kD + 4);  // records of head h, piece 0
+        float res = 0.f;
+        if (cnp > 0) {
+            // lane j: piece j's running max and sum
+            const int j = lane;
+            bool has = false;
+            float mj = -INFINITY, lj = 0.f;
+            if (j < cW) {
+                const int lo_j = static_cast<int>(static_cast<int64_t>(j) * cP / cW);
+                const int hi_j = min(static_cast<int>(static_cast<int64_t>(j + 1) * cP / cW), cnp);
+                has = lo_j < hi_j;
+                if (has) {
+                    mj = rb[j * (kD + 4)];
+                    lj = rb[j * (kD + 4) + 1];
+                }
+            }
+            float M = mj;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            const bool bad = __any_sync(0xffffffffu, has && lj < 0.f);
+            const float fj = has ? ptx::ex2(mj - M) : 0.f;
+            float L = fj * lj;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+            // accumulators: every piece's value at this lane's head_dim index
+            float acc = 0.f;
+            const float *vp = rb + 4 + 32 * ch + lane;
+#pragma unroll 4
+            for (int jj = 0; jj < cW; ++jj) {
+                const float f = __shfl_sync(0xffffffffu, fj, jj);
+                if (f != 0.f) acc += f * vp[jj * (kD + 4)];
+            }
+            res = bad ? 0.f : acc / L;
+        }
+        p.out[(static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD + 32 * ch + lane] = res;
+    }
+    }
 }
 
 // Split-context reduce.  Tasks are (item, query head); a warp takes tasks
@@ -1033,7 +1164,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
 // piece, then the accumulators four pieces per batch).  Lanes run across
 // head_dim; pieces are combined in a fixed order.
 constexpr int kRedThreads = 128;
-constexpr int kRedCtasPerSm = 4;  // a grid that fits in one wave once the decode is gone
 
 template <int kD>
 __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const DecodeArgs p)
@@ -1174,21 +1304,49 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const DecodeArgs p)
 // Launch with programmatic stream serialisation: the kernel may begin while
 // the previous kernel on the stream drains; it calls griddepcontrol.wait
 // before touching that kernel's results.
+// cluster > 0: thread-block clusters of that many CTAs.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
-                       cudaStream_t st, Args &&...args)
+                       cudaStream_t st, int cluster, Args &&...args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster > 0 ? cluster : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster > 0 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// How many clusters of `cluster` CTAs of kern can be resident at once.
+template <typename... KArgs>
+int cluster_capacity(void (*kern)(KArgs...), size_t smem, int cluster)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 // ------------------------------------------------------------------- host
@@ -1253,6 +1411,14 @@ struct OccCache {
     int per_sm = 0;
 };
 
+// Resident clusters of `cl` CTAs with `smem` bytes each, recently asked.
+struct ClusterCache {
+    int device = -1;
+    size_t smem = 0;
+    int cl = 0;
+    int clusters = 0;
+};
+
 template <int kKv, int kD, bool kLoCols>
 pkv_status launch(const DecodeCall &call, const Shape &sh)
 {
@@ -1261,17 +1427,32 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     if (!current_device_info(&di)) return PKV_ERR_CUDA;
     const size_t smem = C::smem_bytes(call.num_seqs);
     if (smem > di.max_smem_optin) return PKV_ERR_UNSUPPORTED;
-    auto kern = decode_kernel<kKv, kD, kLoCols>;
+    auto kern = decode_kernel<kKv, kD, kLoCols, false>;
+    auto kern_cl = decode_kernel<kKv, kD, kLoCols, true>;
     static OccCache occ[64];
+    static size_t smem_attr[2][64] = {};  // dynamic shared memory each kernel may use, per device
+    static ClusterCache ccache[8];
+    static int ccache_next = 0;
+    size_t smem_launch = smem;
     int per_sm = 0;
     int cap = 0;
+    int clust = 0;
     {
         std::lock_guard<std::mutex> lock(g_cfg_mu);
         OccCache &oc = occ[di.device & 63];
+        // raise a kernel's dynamic shared memory limit to what a launch needs
+        auto allow = [&](auto k, int which, size_t bytes) -> bool {
+            if (bytes <= smem_attr[which][di.device & 63]) return true;
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(bytes)) != cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+            smem_attr[which][di.device & 63] = bytes;
+            return true;
+        };
+        if (!allow(kern, 0, smem)) return PKV_ERR_CUDA;
         if (oc.device != di.device || oc.smem != smem) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)) != cudaSuccess)
-                return PKV_ERR_CUDA;
             int v = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, smem) !=
                 cudaSuccess)
@@ -1282,6 +1463,43 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
         }
         per_sm = oc.per_sm;
         cap = g_worker_cap;
+        // One item per cluster when every item's cluster fits in one wave
+        // (and no worker cap asks for the persistent partition): the
+        // cluster's warps split the item's pages, about one stage each as
+        // far as the wave allows, and merge through distributed shared
+        // memory, with no reduce launch.
+        const int64_t items = static_cast<int64_t>(call.num_seqs) * sh.items_per_seq;
+        const int64_t resident = static_cast<int64_t>(per_sm) * di.num_sms;
+        const int64_t stage_pages = static_cast<int64_t>(kWarps) * C::kPPS;
+        const int64_t pages = (sh.ctx_cap + kPage - 1) / kPage;
+        int64_t cl = (pages + stage_pages - 1) / stage_pages;
+        if (cl > kMaxCluster) cl = kMaxCluster;
+        if (items > 0 && cl > resident / items) cl = resident / items;
+        // the records pushed to a CTA take shared memory, so a smaller
+        // cluster may be what fits in one wave: halve until it does
+        for (; cap == 0 && cl >= 1 && items * cl <= resident; cl = cl > 1 ? cl / 2 : 0) {
+            const int hpc = static_cast<int>((sh.rec_heads + cl - 1) / cl);
+            const size_t smem_cl = 1024 + C::crec_offset(call.num_seqs) +
+                                   C::crec_bytes(static_cast<int>(cl) * kWarps, hpc);
+            if (smem_cl > di.max_smem_optin || !allow(kern_cl, 1, smem_cl)) continue;
+            int fit = -1;
+            for (const ClusterCache &e : ccache)
+                if (e.device == di.device && e.smem == smem_cl && e.cl == cl) fit = e.clusters;
+            if (fit < 0) {
+                fit = cluster_capacity(kern_cl, smem_cl, static_cast<int>(cl));
+                ClusterCache &e = ccache[ccache_next];
+                ccache_next = (ccache_next + 1) % 8;
+                e.device = di.device;
+                e.smem = smem_cl;
+                e.cl = static_cast<int>(cl);
+                e.clusters = fit;
+            }
+            if (fit >= items) {
+                clust = static_cast<int>(cl);
+                smem_launch = smem_cl;
+                break;
+            }
+        }
     }
     if (per_sm <= 0) return PKV_ERR_UNSUPPORTED;
     int64_t workers = static_cast<int64_t>(per_sm) * di.num_sms * kWarps;
@@ -1324,11 +1542,22 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     args.num_blocks = call.num_blocks;
     args.ctx_cap = sh.ctx_cap;
     args.num_workers = static_cast<int>(workers);
+    args.clust = clust;
     args.scale_log2 = call.softmax_scale * 1.4426950408889634f;
 
     cudaStream_t st = static_cast<cudaStream_t>(call.stream);
+    if (clust) {
+        const int64_t items = static_cast<int64_t>(call.num_seqs) * sh.items_per_seq;
+        args.num_workers = static_cast<int>(items * clust * kWarps);
+        if (launch_pdl(kern_cl, static_cast<unsigned>(items * clust), kThreads, smem_launch, st, clust,
+                       args, tmk, tmv) != cudaSuccess) {
+            cudaGetLastError();
+            return PKV_ERR_CUDA;
+        }
+        return PKV_OK;
+    }
     const unsigned grid = static_cast<unsigned>((workers + kWarps - 1) / kWarps);
-    if (launch_pdl(kern, grid, kThreads, smem, st, args, tmk, tmv) != cudaSuccess) {
+    if (launch_pdl(kern, grid, kThreads, smem, st, 0, args, tmk, tmv) != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }
@@ -1337,23 +1566,38 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
         const int64_t tasks =
             static_cast<int64_t>(call.num_seqs) * sh.items_per_seq * sh.rec_heads;
         int64_t rgrid = (tasks + kRedWarps - 1) / kRedWarps;
-        if (rgrid > static_cast<int64_t>(kRedCtasPerSm) * di.num_sms)
-            rgrid = static_cast<int64_t>(kRedCtasPerSm) * di.num_sms;
         const size_t rsmem = static_cast<size_t>(2 * call.num_seqs + 1) * sizeof(int32_t);
         auto rk = reduce_kernel<kD>;
+        int red_per_sm = 0;
         {
-            // the per-sequence tables of the largest batch, once per device
+            // the per-sequence tables of the largest batch, once per device;
+            // a grid of at most one wave (warps then loop over the tasks)
             static int red_ready[64] = {};
+            static size_t red_smem[64] = {};
+            static int red_occ[64] = {};
             std::lock_guard<std::mutex> lock(g_cfg_mu);
-            if (!red_ready[di.device & 63]) {
+            const int dv = di.device & 63;
+            if (!red_ready[dv]) {
                 if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>((2 * kMaxSeqs + 1) * sizeof(int32_t))) !=
                     cudaSuccess)
                     return PKV_ERR_CUDA;
-                red_ready[di.device & 63] = 1;
+                red_ready[dv] = 1;
+                red_smem[dv] = ~size_t(0);
             }
+            if (red_smem[dv] != rsmem) {
+                int v = 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, rk, kRedThreads, rsmem) !=
+                    cudaSuccess)
+                    return PKV_ERR_CUDA;
+                red_smem[dv] = rsmem;
+                red_occ[dv] = v;
+            }
+            red_per_sm = red_occ[dv];
         }
-        if (launch_pdl(rk, static_cast<unsigned>(rgrid), kRedThreads, rsmem, st, args) !=
+        const int64_t wave = static_cast<int64_t>(red_per_sm > 0 ? red_per_sm : 1) * di.num_sms;
+        if (rgrid > wave) rgrid = wave;
+        if (launch_pdl(rk, static_cast<unsigned>(rgrid), kRedThreads, rsmem, st, 0, args) !=
             cudaSuccess) {
             cudaGetLastError();
             return PKV_ERR_CUDA;

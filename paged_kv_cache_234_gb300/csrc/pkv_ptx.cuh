@@ -259,6 +259,16 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t local, uint32_t rank)
     return remote;
 }
 
+// Generic address of the location in CTA `rank`'s shared memory that the
+// shared-memory generic address p has in this CTA; ordinary loads and stores
+// through it reach the other CTA (distributed shared memory).
+__device__ __forceinline__ void *map_generic(void *p, uint32_t rank)
+{
+    uint64_t r;
+    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+    return reinterpret_cast<void *>(r);
+}
+
 __device__ __forceinline__ uint32_t ld_cluster_addr(uint32_t cluster_addr)
 {
     uint32_t v;

@@ -22,6 +22,25 @@ def ensure_built():
         _built = True
 
 
+class persistent_workers:
+    """Within the block, decode calls use the persistent-worker partition
+    (split-context pieces merged by the reduce kernel) even for batches that
+    would take the one-item-per-cluster launch: a worker cap set through
+    pkv_set_decode_workers selects the persistent partition."""
+
+    def __init__(self, cap=4096):
+        self.cap = cap
+
+    def __enter__(self):
+        ensure_built()
+        pkv.pkv_set_decode_workers(self.cap)
+        return self
+
+    def __exit__(self, *exc):
+        pkv.pkv_set_decode_workers(0)
+        return False
+
+
 def dev(a, dtype=None):
     t = torch.from_numpy(np.ascontiguousarray(a))
     if dtype is not None:

@@ -11,7 +11,7 @@ import torch
 import paged_kv_cache_234_gb300 as pkv
 import pkv_workloads as W
 from gpu_common import (assert_close, dev, ensure_built, gpu_decode, oracle_codes,
-                        oracle_decode)
+                        oracle_decode, persistent_workers)
 
 pytestmark = pytest.mark.gpu
 
@@ -66,23 +66,31 @@ def test_split_count_sweep(variant, workers):
     assert diff <= 1e-6
 
 
+@pytest.mark.parametrize("mode", ["auto", "persistent"])
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (8, 2, 64), (14, 2, 64), (32, 8, 128),
                                       (16, 1, 128), (24, 2, 64), (4, 4, 64)])
-def test_group_sizes_and_edge_lengths(variant, hq, hkv, d):
+def test_group_sizes_and_edge_lengths(variant, hq, hkv, d, mode):
+    # "auto": these small batches take the one-item-per-cluster launch;
+    # "persistent": the same batch through the persistent workers + reduce
     lens = [1, 15, 16, 17, 0, 33, 255, 256, 257]
     w = W.random_case(7 * hq + d, num_seqs=len(lens), num_heads=hq, num_kv_heads=hkv,
                       head_dim=d, context_lens=lens)
     codes = oracle_codes(w, variant == "fp8")
-    got, st = gpu_decode(w, variant, codes)
+    if mode == "persistent":
+        with persistent_workers():
+            got, st = gpu_decode(w, variant, codes)
+    else:
+        got, st = gpu_decode(w, variant, codes)
     ref, flags = oracle_decode(w, variant, codes)
     assert st == 0 and not flags.any()
     assert_close(got, ref, f"{hq}/{hkv}/{d}")
     assert np.all(got[4] == 0)  # empty context
 
 
+@pytest.mark.parametrize("mode", ["auto", "persistent"])
 @pytest.mark.parametrize("variant", VARIANTS)
-def test_bad_block_id_and_bad_length_give_zeros_and_status(variant):
+def test_bad_block_id_and_bad_length_give_zeros_and_status(variant, mode):
     w = W.random_case(55, num_seqs=5, num_heads=8, num_kv_heads=2, head_dim=64,
                       context_lens=[40, 100, 64, 5, 70])
     codes = oracle_codes(w, variant == "fp8")
@@ -91,7 +99,12 @@ def test_bad_block_id_and_bad_length_give_zeros_and_status(variant):
     tables[4, 2] = -7
     lens = w.context_lens.copy()
     lens[2] = 10_000                     # beyond max_context_len
-    got, st = gpu_decode(w, variant, codes, max_context_len=100, tables=tables, lens=lens)
+    if mode == "persistent":
+        with persistent_workers():
+            got, st = gpu_decode(w, variant, codes, max_context_len=100, tables=tables,
+                                 lens=lens)
+    else:
+        got, st = gpu_decode(w, variant, codes, max_context_len=100, tables=tables, lens=lens)
     ref, flags = oracle_decode(w, variant, codes, max_context_len=100, tables=tables, lens=lens)
     assert st == pkv.PKV_DEV_BAD_BLOCK | pkv.PKV_DEV_BAD_CTX
     for s in (1, 2, 4):
@@ -117,3 +130,22 @@ def test_all_empty_contexts_write_zeros():
                       context_lens=[0, 0, 0])
     got, st = gpu_decode(w, "fp16", max_context_len=0)
     assert st == 0 and np.all(got == 0)
+    with persistent_workers():
+        got, st = gpu_decode(w, "fp16", max_context_len=0)
+    assert st == 0 and np.all(got == 0)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["c1_tiny", "c2_8x512", "c4_qwen2_b8"])
+def test_small_configs_both_launches_agree(name, variant):
+    # the one-item-per-cluster launch and the persistent workers + reduce give
+    # the oracle's answer and agree with each other to float rounding
+    w, codes = workload(name, variant)
+    got, st = gpu_decode(w, variant, codes)
+    with persistent_workers():
+        alt, st2 = gpu_decode(w, variant, codes)
+    ref, _ = oracle_decode(w, variant, codes)
+    assert st == 0 and st2 == 0
+    assert_close(got, ref, f"{name}/{variant} cluster")
+    assert_close(alt, ref, f"{name}/{variant} persistent")
+    assert float(np.max(np.abs(got - alt))) <= 1e-6
