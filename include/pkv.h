@@ -22,7 +22,12 @@
  *         scaled FP8 KV).
  *
  * Layouts (all row-major, all pointers are DEVICE pointers owned by the
- * caller; the library never allocates, frees or synchronises):
+ * caller; the library never allocates, frees or synchronises).  A decode
+ * call's query, block_tables, context_lens and out, and the quantizers'
+ * block_ids, may also be pinned host memory (page-locked, e.g. from
+ * cudaHostAlloc: one address for the host and the GPU), which the kernels
+ * then read or write in place over the GPU's link to the host; KV pools,
+ * scales and workspaces must be device memory:
  *   K/V pools      [num_blocks][num_kv_heads][block_size][head_dim]
  *                  (one contiguous tile per (block, kv head))
  *   scales         [num_blocks][num_kv_heads]  fp32, one for K, one for V

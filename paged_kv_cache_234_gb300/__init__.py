@@ -178,11 +178,15 @@ def _stream(stream) -> Optional[int]:
     return torch.cuda.current_stream().cuda_stream
 
 
-def _check(t, name, dtype=None):
+def _check(t, name, dtype=None, host_ok=False):
+    """host_ok: a pinned host tensor is accepted as well (the GPU reads or
+    writes it in place over its link to the host; pinned memory has one
+    address for the host and the GPU)."""
     if t is None:
         return
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" +
+                         (" or a pinned host tensor" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -224,7 +228,7 @@ def _quantize(fn_name, k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, blo
     _check(v_codes, "v_codes", code_t)
     _check(k_scales, "k_scales", torch.float32)
     _check(v_scales, "v_scales", torch.float32)
-    _check(block_ids, "block_ids", torch.int32)
+    _check(block_ids, "block_ids", torch.int32, host_ok=True)
     _check(dev_status, "dev_status", torch.int32)
     nb, hkv, bs, d = k_fp16.shape
     nids = 0 if block_ids is None else block_ids.numel()
@@ -239,10 +243,11 @@ def _quantize(fn_name, k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, blo
 def _decode(fn_name, out, query, kp, vp, ks, vs, block_tables, context_lens,
             max_context_len, softmax_scale, workspace, dev_status, stream):
     import torch
-    _check(out, "out", torch.float32)
-    _check(query, "query", torch.float16)
-    _check(block_tables, "block_tables", torch.int32)
-    _check(context_lens, "context_lens", torch.int32)
+    # the per-step inputs and the output may live in pinned host memory
+    _check(out, "out", torch.float32, host_ok=True)
+    _check(query, "query", torch.float16, host_ok=True)
+    _check(block_tables, "block_tables", torch.int32, host_ok=True)
+    _check(context_lens, "context_lens", torch.int32, host_ok=True)
     _check(workspace, "workspace")
     _check(dev_status, "dev_status", torch.int32)
     n, hq, d = query.shape
