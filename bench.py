@@ -48,7 +48,7 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2: written, then another one read, between 
 # DRAM bytes per launch of the INT8 decode (decode + reduce kernels) on this
 # workload from the ncu capture summarised in profiles/, with the hash of the
 # kernel source it was taken on; the figure is dropped when the source changes.
-TRAFFIC = {"decode_int8": (272039168 + 5051520, "5861261160063347")}  # decode + reduce kernels
+TRAFFIC = {"decode_int8": (270961408 + 5002496, "82ec6c1e5006ebb0")}  # decode + reduce kernels
 
 
 def _src_hash():
@@ -296,8 +296,11 @@ def run_profile(args):
     import paged_kv_cache_234_gb300 as pkv
     from paged_kv_cache_234_gb300 import build as pkv_build
     pkv_build.build()
-    w = W.build(CONFIG + "_pool16k", num_heads=32, num_kv_heads=8, head_dim=128,
-                num_blocks=16384, context_lens=[2048] * 64, seed=1005)
+    if args.profile == "int8-small":
+        w = W.make("c2_8x512")
+    else:
+        w = W.build(CONFIG + "_pool16k", num_heads=32, num_kv_heads=8, head_dim=128,
+                    num_blocks=16384, context_lens=[2048] * 64, seed=1005)
     n, hq, d = w.query.shape
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     kf, vf = dev(w.k_pool), dev(w.v_pool)
@@ -311,7 +314,7 @@ def run_profile(args):
         vs = torch.zeros_like(ks)
         tails = dev(w.tail_block_ids())
         call = lambda: pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, tails)
-    elif args.profile in ("int8", "fp8"):
+    elif args.profile in ("int8", "fp8", "int8-small"):
         kc = torch.zeros(w.k_pool.shape, dtype=torch.int8, device="cuda")
         vc = torch.zeros_like(kc)
         ks = torch.zeros(w.k_pool.shape[:2], dtype=torch.float32, device="cuda")
@@ -385,7 +388,8 @@ def run_report(args):
     fw = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     fr = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    for name in W.CONFIG_NAMES:
+    names = [c for c in args.configs.split(",") if c] or list(W.CONFIG_NAMES)
+    for name in names:
         w = W.make(name)
         n, hq, d = w.query.shape
         hkv = w.num_kv_heads
@@ -496,10 +500,15 @@ def main():
                          "line each (no benchmark line)")
     ap.add_argument("--report-warmup", type=int, default=20)
     ap.add_argument("--report-calls", type=int, default=200)
-    ap.add_argument("--profile", choices=["int8", "fp8", "fp16", "quantize", "append", "evict"],
+    ap.add_argument("--configs", default="",
+                    help="with --report-configs: comma-separated configuration names to "
+                         "report (default: all)")
+    ap.add_argument("--profile", choices=["int8", "fp8", "fp16", "quantize", "append", "evict",
+                                          "int8-small"],
                     help="profiling run: the same batch over a 16384-block pool (eviction: "
-                         "a 65536-block pool), only warm-up + timed calls of one kernel, "
-                         "no report line")
+                         "a 65536-block pool; int8-small: the 8 x 512 batch, whose INT8 "
+                         "decode takes the one-item-per-cluster launch), only warm-up + "
+                         "timed calls of one kernel, no report line")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
