@@ -8,10 +8,11 @@
  *
  * Sources for what each call computes:
  *  [PKF]  "PagedKV-Fusion" README (INT8 per-(block, head) quantized decode
- *         attention): "Overview" component B, "Architecture" flowchart
- *         ("per-block,head symmetric INT8", "online softmax . GQA") and
- *         sequence diagram ("INT8 survivors + scales", "decode step (block
- *         table)"), "Memory footprint" table.
+ *         attention): Overview, component B; Architecture, the flowchart
+ *         (symmetric INT8 per block and head; online softmax with GQA) and
+ *         the sequence diagram (INT8 codes handed on with their scales; the
+ *         decode step through the block table); Results, Memory footprint
+ *         table.
  *  [PAR]  "paged-attention-runtime" summary: CORE CAPABILITIES 1 (16-token
  *         blocks) and 2 (block-table indirection, online softmax, FP32
  *         accumulation), 4 (GQA).
@@ -83,8 +84,8 @@ typedef enum pkv_status {
 
 /*
  * pkv_quantize_blocks -- symmetric per-(block, kv head) INT8 quantization
- * of fp16 K and V tiles ([PKF] Overview component B; sequence diagram
- * "INT8 survivors + scales").
+ * of fp16 K and V tiles ([PKF] Overview, component B; Architecture, sequence
+ * diagram: INT8 codes handed on with their scales).
  *
  * For every listed block b and kv head h, separately for K and V, over all
  * block_size * head_dim values x of the tile (padding slots included):
@@ -116,8 +117,8 @@ PKV_API pkv_status pkv_quantize_blocks(const void *k_fp16, const void *v_fp16,
 
 /*
  * pkv_paged_decode_fp16 -- one decode step of paged attention over fp16 KV
- * ([PKF] sequence diagram "decode step (block table)"; [PAR] CORE
- * CAPABILITIES 2 and 4; [GLO] section 2.1).
+ * ([PKF] Architecture, sequence diagram: the decode step through the block
+ * table; [PAR] CORE CAPABILITIES 2 and 4; [GLO] section 2.1).
  *
  * For every sequence s (ctx = context_lens[s]) and query head h with kv head
  * kvh = h / (num_heads / num_kv_heads):
@@ -156,7 +157,7 @@ PKV_API pkv_status pkv_paged_decode_fp16(float *out, const void *query,
 /*
  * pkv_paged_decode_int8 -- the same decode step over INT8 KV with one fp32
  * scale per (block, kv head) for K and one for V ([PKF] Overview component
- * B, "Architecture" flowchart): K_t = k_codes[...] * k_scales[blk][kvh],
+ * B; Architecture, flowchart): K_t = k_codes[...] * k_scales[blk][kvh],
  * V_t = v_codes[...] * v_scales[blk][kvh], as produced by
  * pkv_quantize_blocks.  Arguments as for pkv_paged_decode_fp16, with
  *   k_codes/v_codes  int8 pools, 16-byte aligned
@@ -228,7 +229,10 @@ PKV_API pkv_status pkv_paged_decode_fp8(float *out, const void *query,
  *    that loads the library holds PKV_STATIC_WORKSPACE_BYTES until exit;
  *  - the first call on each device looks up the array's device address
  *    (with that device current); make that first call before any stream
- *    capture begins;
+ *    capture begins.  The address is kept for the life of the process, so
+ *    resetting the device (cudaDeviceReset, or anything else that destroys
+ *    its primary context) after that first call is not supported while the
+ *    library stays loaded;
  *  - a call whose workspace requirement (pkv_decode_workspace_size) exceeds
  *    PKV_STATIC_WORKSPACE_BYTES returns PKV_ERR_WORKSPACE without launching;
  *  - all calls on a device share the one array: calls that can overlap on
@@ -251,11 +255,11 @@ PKV_API pkv_status pkv_paged_decode_int8_static_workspace(
  * sequence s with t = positions[s] >= 0, row t % 16 of tile
  * (block_tables[s][t / 16], kv head h) of each pool is set to
  * k_new[s][h][:] / v_new[s][h][:], for every kv head h
- * ([GLO] section 2.1 "Logical Token Blocks & Page Tables": block = table[t /
- * B], slot = t % B; "Kernel Mechanics": each token is written at
- * phys_block_id * B + token_offset; section 3.3.2: "append the delta
- * tokens").  A decode over context_lens[s] = t + 1 then attends to the new
- * token.
+ * ([GLO] section 2.1, Logical Token Blocks & Page Tables: block = table[t /
+ * B], slot = t % B, and under Kernel Mechanics the write of a token to slot
+ * phys_block_id * B + token_offset; section 3.3.2: new tokens are appended
+ * to the cache).  A decode over context_lens[s] = t + 1 then attends to the
+ * new token.
  *
  *   k_cache, v_cache  fp16 pools [num_blocks][num_kv_heads][16][head_dim],
  *                     written in place, 16-byte aligned
@@ -283,7 +287,7 @@ PKV_API pkv_status pkv_append_fp16(void *k_cache, void *v_cache, int num_blocks,
  * every (block, kv head) tile that received a row is re-quantized into
  * k_codes/v_codes and k_scales/v_scales, bit-identical to
  * pkv_quantize_blocks on that block after the fp16 append (one fused kernel;
- * [PKF] sequence diagram "INT8 survivors + scales").  All 16 slots of the
+ * [PKF] Architecture, sequence diagram: INT8 codes with their scales).  All 16 slots of the
  * tile are quantized, as pkv_quantize_blocks does.  Extra arguments:
  *   k_codes, v_codes   int8 pools, 16-byte aligned
  *   k_scales, v_scales fp32 [num_blocks][num_kv_heads], 4-byte aligned
@@ -311,9 +315,10 @@ PKV_API pkv_status pkv_append_fp8(void *k_cache, void *v_cache, uint8_t *k_codes
 
 /*
  * pkv_evict_select -- score every physical block for eviction and choose
- * the k most evictable ones, in one launch ([PKF] Overview component A
- * "Eviction score: fused scoring + top-k over paged KV blocks", sequence
- * diagram "score all physical blocks" -> "eviction ids").  The score is the
+ * the k most evictable ones, in one launch ([PKF] Overview, component A:
+ * eviction scoring of the paged KV blocks fused with the top-k choice;
+ * Architecture, sequence diagram: every physical block scored, the ids to
+ * evict handed back).  The score is the
  * least-reference-count + age heuristic of [GLO] section 4.3.1:
  *   score[b] = alpha * (max_refcnt - refcnt[b]) + beta * (current_tick - last_used[b])
  * evaluated in fp32, one rounding per operation, each difference formed

@@ -24,8 +24,22 @@ from gpu_common import assert_close, dev, ensure_built, oracle_codes, oracle_dec
 pytestmark = pytest.mark.gpu
 
 
-def test_matches_the_workspace_entry_point_on_two_calls_in_a_row():
+@pytest.mark.parametrize("launch", ["auto", "persistent"])
+def test_matches_the_workspace_entry_point_on_two_calls_in_a_row(launch):
+    # "persistent": a worker cap selects the persistent workers + reduce,
+    # whose split-context records live in the scratch array; "auto": this
+    # batch's own choice (it fits one item per thread-block cluster, which
+    # merges in shared memory and uses no scratch)
     ensure_built()
+    if launch == "persistent":
+        pkv.pkv_set_decode_workers(4096)
+    try:
+        _two_calls_in_a_row()
+    finally:
+        pkv.pkv_set_decode_workers(0)
+
+
+def _two_calls_in_a_row():
     w = W.random_case(91, num_seqs=16, num_heads=32, num_kv_heads=8, head_dim=128, max_ctx=1500)
     codes = oracle_codes(w)
     kc, vc, ks, vs = (dev(x) for x in codes)
