@@ -138,12 +138,18 @@ __device__ __forceinline__ int64_t dbg_index(int64_t i, int64_t n)
 __device__ unsigned long long g_debug_stage_wait_ns = kWaitLimitNs;
 #define PKV_STAGE_WAIT_NS g_debug_stage_wait_ns
 #define PKV_SMEM(addr, bytes, align) dbg_smem((addr), (bytes), (align))
+// a shared-memory record reached through a generic pointer (one item per
+// cluster): its range inside the CTA's dynamic shared memory
+#define PKV_REC(ptr, bytes)                                                              \
+    reinterpret_cast<float *>(__cvta_shared_to_generic(                                  \
+        dbg_smem(static_cast<uint32_t>(__cvta_generic_to_shared(ptr)), (bytes), 16)))
 #define PKV_IDX(i, n) dbg_index((i), (n))
 #define PKV_TABLE_AT(p, seq, page, u, mb) \
     ((p).block_tables + dbg_index((seq), (p).num_seqs) * (mb) + dbg_index((page) + (u), (mb)))
 #else
 #define PKV_STAGE_WAIT_NS kWaitLimitNs
 #define PKV_SMEM(addr, bytes, align) (addr)
+#define PKV_REC(ptr, bytes) (ptr)
 #define PKV_IDX(i, n) (i)
 #define PKV_TABLE_AT(p, seq, page, u, mb) ((p).block_tables + (seq) * (mb) + (page) + (u))
 #endif
@@ -616,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     float *crec = reinterpret_cast<float *>(smem + C::crec_offset(p.num_seqs));
     auto crec_of = [&](int h) -> float * {
         const int slot = (h / p.clust) * cW + cw;
-        return static_cast<float *>(ptx::map_generic(crec + slot * (kD + 4), h % p.clust));
+        float *local = PKV_REC(crec + slot * (kD + 4), (kD + 4) * 4);
+        return static_cast<float *>(ptx::map_generic(local, h % p.clust));
     };
     if constexpr (kClust) {
         const int r = static_cast<int>(ptx::cluster_ctarank());
@@ -1124,8 +1131,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
                 const int hi_j = min(static_cast<int>(static_cast<int64_t>(j + 1) * cP / cW), cnp);
                 has = lo_j < hi_j;
                 if (has) {
-                    mj = rb[j * (kD + 4)];
-                    lj = rb[j * (kD + 4) + 1];
+                    const float *rj = PKV_REC(const_cast<float *>(rb) + j * (kD + 4), (kD + 4) * 4);
+                    mj = rj[0];
+                    lj = rj[1];
                 }
             }
             float M = mj;

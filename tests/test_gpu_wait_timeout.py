@@ -13,7 +13,10 @@ a wait is one non-blocking test of the barrier, and a copy still in flight
 counts as timed out.  The copies themselves do land, and the drain after the
 timeout waits for them with its normal limit.  After the limit is restored,
 the same call on the debug build and on the release build matches the
-oracle again.
+oracle again.  Both launches are covered: this batch's own one (one item per
+thread-block cluster, where a warp that gave up still joins its cluster's
+barrier and marks its records bad) and the persistent workers + reduce
+(selected by a worker cap).
 """
 import numpy as np
 import pytest
@@ -45,26 +48,35 @@ def _debug_int8(L, w, codes):
     return rc, out.cpu().numpy().astype(np.float64), int(status.item())
 
 
-def test_a_stage_wait_that_runs_out_sets_the_status_and_the_call_returns():
+@pytest.mark.parametrize("launch", ["auto", "persistent"])
+def test_a_stage_wait_that_runs_out_sets_the_status_and_the_call_returns(launch):
     ensure_built()
     L = pkv.debug_lib()
+    cap = 4096 if launch == "persistent" else 0
     w = W.random_case(93, num_seqs=16, num_heads=32, num_kv_heads=8, head_dim=128,
                       max_ctx=1500)
     codes = oracle_codes(w)
     ref, _ = oracle_decode(w, "int8", codes)
     try:
+        assert L.pkv_set_decode_workers(cap) == 0
         assert L.pkv_debug_set_stage_wait_ns(0) == 0
         rc, _, st = _debug_int8(L, w, codes)
         assert rc == 0
         assert st & pkv.PKV_DEV_TIMEOUT, f"status {st:#x}: no stage wait ran out"
     finally:
         assert L.pkv_debug_set_stage_wait_ns(-1) == 0
-    assert L.pkv_debug_flags(1) == 0  # the timed-out run stayed inside its buffers
-
-    # the same call with the default limit, on the debug and the release build
-    rc, got, st = _debug_int8(L, w, codes)
-    assert rc == 0 and st == 0
-    assert_close(got, ref, "debug build after the timeout")
-    got, st = gpu_decode(w, "int8", codes)
+    try:
+        assert L.pkv_debug_flags(1) == 0  # the timed-out run stayed inside its buffers
+        # the same call with the default limit, on the debug and the release build
+        rc, got, st = _debug_int8(L, w, codes)
+        assert rc == 0 and st == 0
+        assert_close(got, ref, f"debug build after the timeout ({launch})")
+    finally:
+        L.pkv_set_decode_workers(0)
+    pkv.pkv_set_decode_workers(cap)
+    try:
+        got, st = gpu_decode(w, "int8", codes)
+    finally:
+        pkv.pkv_set_decode_workers(0)
     assert st == 0
-    assert_close(got, ref, "release build after the timeout")
+    assert_close(got, ref, f"release build after the timeout ({launch})")
