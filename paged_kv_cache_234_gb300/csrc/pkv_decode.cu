@@ -1144,13 +1144,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             float L = fj * lj;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-            // accumulators: every piece's value at this lane's head_dim index
+            // accumulators: every piece's value at this lane's head_dim
+            // index, eight pieces' loads in flight at a time
             float acc = 0.f;
             const float *vp = rb + 4 + 32 * ch + lane;
-#pragma unroll 4
-            for (int jj = 0; jj < cW; ++jj) {
-                const float f = __shfl_sync(0xffffffffu, fj, jj);
-                if (f != 0.f) acc += f * vp[jj * (kD + 4)];
+            for (int jb = 0; jb < cW; jb += 8) {
+                float v[8], f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    f[u] = __shfl_sync(0xffffffffu, fj, (jb + u) & 31);
+                    v[u] = jb + u < cW && f[u] != 0.f ? vp[(jb + u) * (kD + 4)] : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) acc += f[u] * v[u];
             }
             res = bad ? 0.f : acc / L;
         }
