@@ -9,8 +9,8 @@ memory), and the worker returns: the call ends and the context stays usable
 
 A copy that never lands cannot be made safely, so the debug build of the
 library (PKV_DEBUG) takes the limit of the stage waits from a setting: at 0
-a wait is one non-blocking test of the barrier, and a copy still in flight
-counts as timed out.  The copies themselves do land, and the drain after the
+a wait gives up at once, as if its limit had run out, while its copies are
+still in flight.  The copies themselves do land, and the drain after the
 timeout waits for them with its normal limit.  After the limit is restored,
 the same call on the debug build and on the release build matches the
 oracle again.  Both launches are covered: this batch's own one (one item per
