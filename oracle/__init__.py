@@ -26,7 +26,7 @@ Every function cites the passage it follows:
 * ``append_fp16`` / ``append_int8`` -- the write of one new token per
   sequence at slot table[s][t / B] * B + t % B ("PagedAttention & KV-Cache
   Memory Management", section 2.1 and the prefill step of its kernel
-  mechanics; section 3.3.2 "append the delta tokens"); the INT8 cache then
+  mechanics; section 3.3.2, each step adding only its new tokens); the INT8 cache then
   re-quantizes every tile it wrote with ``quantize``.
 * ``evict_scores`` / ``evict_select`` -- the least-reference-count + age
   score of "PagedAttention & KV-Cache Memory Management", section 4.3.1

@@ -2,8 +2,8 @@
 // each sequence goes to slot t % 16 of physical block table[s][t / 16]
 // ("PagedAttention & KV-Cache Memory Management", section 2.1 "Logical Token
 // Blocks & Page Tables" and the prefill step of "Kernel Mechanics" that
-// writes each token at phys_block_id * B + token_offset; section 3.3.2
-// "append the delta tokens").
+// writes each token at phys_block_id * B + token_offset; section 3.3.2,
+// where each step adds only the new tokens to the cache).
 //
 // fp16 cache: one thread per 16-byte chunk of a new row; a row of head_dim
 // fp16 values is 8 or 16 threads, so a warp writes 2 or 4 full rows.

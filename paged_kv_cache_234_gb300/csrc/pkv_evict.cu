@@ -6,9 +6,11 @@
 //   score = alpha * (max_refcnt - refcnt) + beta * (current_tick - last_used)
 // in fp32 with one rounding per operation; a larger score is more evictable.
 // Every physical block is scored and the eviction ids are returned
-// (PagedKV-Fusion README: component A "fused scoring + top-k over paged KV
-// blocks" and the sequence diagram's "score all physical blocks" / "eviction
-// ids").  Blocks with refcnt <= 0 are free and are never chosen; max_refcnt is
+// (PagedKV-Fusion README: Overview, component A, a CUDA kernel that scores
+// the blocks and selects k of them in one pass, and the Architecture
+// sequence diagram, where the eviction kernel scores every physical block
+// and returns the ids of the k blocks to evict to its caller).  Blocks with
+// refcnt <= 0 are free and are never chosen; max_refcnt is
 // the largest refcnt of the pool; equal scores go to the smaller block id.
 //
 // GB300 design: one thread-block cluster (up to 16 CTAs of 512 threads) owns

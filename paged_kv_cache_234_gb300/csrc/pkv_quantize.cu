@@ -1,6 +1,7 @@
 // pkv_quantize.cu -- symmetric per-(block, kv head) INT8 quantization of fp16
 // K and V tiles (PagedKV-Fusion README, "Overview" component B and the
-// "Architecture" sequence diagram step "INT8 survivors + scales"), and the
+// "Architecture" sequence diagram, where the blocks kept after eviction are
+// handed on as INT8 codes with their scales), and the
 // same with FP8 (OCP E4M3) codes and scale = amax / 448 ("PagedAttention &
 // KV-Cache Memory Management", section 5.1: per-block scaled FP8 KV).
 //
