@@ -382,8 +382,14 @@ def run_report(args):
     """Per configuration and variant: p50 / p90 us per decode call over 200
     timed calls after 20 warm-ups (--report-calls, --report-warmup), L2
     flushed before each call; KV GB/s of the logical bytes (unique bytes too
-    where sequences share blocks) and sequence-steps/s.  One JSON line per
-    (configuration, variant), in the order the calls run."""
+    where sequences share blocks) and sequence-steps/s.  Beside them, as
+    labelled extras: the GPU time of a call with the L2 flushed before it but
+    without the event pair and host overhead (flush + call pairs replayed
+    from a CUDA graph, minus the flushes alone), and the mean of the same
+    number of calls back to back with no flush (warm L2 for the batches that
+    fit in it; small calls there are bound by the Python binding's ~14 us of
+    host work per call).  One JSON line per (configuration, variant), in the
+    order the calls run."""
     import torch
     import paged_kv_cache_234_gb300 as pkv
     from paged_kv_cache_234_gb300 import build as pkv_build
@@ -393,6 +399,43 @@ def run_report(args):
     fw = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     fr = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
+    l2_bytes = torch.cuda.get_device_properties(0).L2_cache_size
+
+    def graph_cold_call(fn, reps=20, replays=7):
+        # labelled extra: GPU time of one call with the L2 flushed before it,
+        # free of event-pair and host overhead: reps x (flush, call) replayed
+        # from one CUDA graph, minus the same graph without the calls
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.synchronize()
+        graphs = []
+        for with_call in (True, False):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(reps):
+                    fw.zero_()
+                    fr.view(torch.int32).max()
+                    if with_call:
+                        fn()
+            graphs.append(g)
+        med = []
+        for g in graphs:
+            ts = []
+            for i in range(replays + 2):
+                g0 = torch.cuda.Event(enable_timing=True)
+                g1 = torch.cuda.Event(enable_timing=True)
+                g0.record(stream)
+                g.replay()
+                g1.record(stream)
+                g1.synchronize()
+                if i >= 2:
+                    ts.append(g0.elapsed_time(g1) * 1e-3)
+            med.append(statistics.median(ts))
+        del graphs
+        return (med[0] - med[1]) / reps
+
     names = [c for c in args.configs.split(",") if c] or list(W.CONFIG_NAMES)
     for name in names:
         w = W.make(name)
@@ -441,11 +484,27 @@ def run_report(args):
             b = decode_bytes(w.context_lens, hkv, d, eb, sc)
             bu = decode_bytes(uniq_ctx, hkv, d, eb, sc)
             t50, t90 = statistics.median(ts), float(np.percentile(ts, 90))
+            # labelled extra: the same calls back to back, one pair of events
+            # around the run, no flush (warm L2 where the batch fits in it)
+            torch.cuda.synchronize()
+            b0 = torch.cuda.Event(enable_timing=True)
+            b1 = torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(args.report_calls):
+                fn()
+            b1.record(stream)
+            b1.synchronize()
+            tb = b0.elapsed_time(b1) * 1e-3 / args.report_calls
+            tg = graph_cold_call(fn)
             rec = {"config": name, "variant": variant, "p50_us": 1e6 * t50,
                    "p90_us": 1e6 * t90, "mean_us": 1e6 * statistics.mean(ts),
                    "kv_bytes": b, "unique_kv_bytes": bu,
                    "GB/s": b / t50 / 1e9, "frac_of_peak": b / t50 / 1e9 / peak,
-                   "seq_steps_per_s": n / t50}
+                   "seq_steps_per_s": n / t50,
+                   "graph_cold_us": 1e6 * tg,
+                   "back_to_back_us": 1e6 * tb,
+                   "back_to_back_l2": "inputs larger than L2" if bu > l2_bytes
+                                      else "warm L2: the batch's KV fits in L2"}
             if variant == "int8" and cpu is not None:
                 rec["cpu_oracle"] = {**cpu, "us_scaled": 1e6 * b / (cpu["GB/s"] * 1e9)}
             print(json.dumps(rec), flush=True)
