@@ -21,6 +21,12 @@ The functions carry the C names and take torch tensors:
 * ``pkv_copy_blocks``         the batched block copies copy-on-write asks for
 * ``pkv_decode_workspace_size``, ``pkv_set_decode_workers``,
   ``pkv_status_string``
+
+``prepare_paged_decode_fp16`` / ``_int8`` / ``_fp8`` and
+``prepare_quantize_blocks`` / ``_fp8`` take the same arguments as the calls
+above and return a ``PreparedCall``: the arguments checked and marshalled
+once, each call of the object issuing the same C call again (for serving
+loops that update the same buffers in place every step).
 """
 from __future__ import annotations
 
@@ -207,19 +213,71 @@ def pkv_set_decode_workers(max_workers: int) -> None:
 def pkv_quantize_blocks(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
                         block_ids=None, dev_status=None, stream=None) -> None:
     """Quantize the (block, kv head) tiles of fp16 pools [NB][Hkv][16][d]."""
-    _quantize("pkv_quantize_blocks", k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
-              block_ids, dev_status, stream)
+    _invoke(*_quantize("pkv_quantize_blocks", k_fp16, v_fp16, k_codes, v_codes, k_scales,
+                       v_scales, block_ids, dev_status, stream))
 
 
 def pkv_quantize_blocks_fp8(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
                             block_ids=None, dev_status=None, stream=None) -> None:
     """FP8 (E4M3, uint8 code pools) quantization of the tiles of fp16 pools."""
-    _quantize("pkv_quantize_blocks_fp8", k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
-              block_ids, dev_status, stream)
+    _invoke(*_quantize("pkv_quantize_blocks_fp8", k_fp16, v_fp16, k_codes, v_codes, k_scales,
+                       v_scales, block_ids, dev_status, stream))
+
+
+def _invoke(fn_name, args):
+    st = getattr(lib(), fn_name)(*args)
+    if st != PKV_OK:
+        raise PkvError(st, fn_name)
+
+
+class PreparedCall:
+    """One call of the C ABI with its arguments checked and marshalled once.
+
+    Calling the object issues the same call again: the same buffers (by
+    address; their contents may change between calls, as a serving loop
+    updates its query, block tables and context lengths in place), the same
+    sizes and the stream that was current (or given) at preparation.  The
+    buffers must stay alive and must not be reallocated while the object is
+    used (the object holds references to the tensors it was prepared with,
+    so they are not freed while it lives).  It saves the per-call argument
+    checks of the plain functions, about ten microseconds of host time per
+    call."""
+
+    __slots__ = ("_fn", "_args", "_name", "_keep")
+
+    def __init__(self, fn_name, args, keep=()):
+        self._fn = getattr(lib(), fn_name)
+        self._args = tuple(args)
+        self._name = fn_name
+        self._keep = tuple(keep)
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != PKV_OK:
+            raise PkvError(st, self._name)
+
+
+def prepare_quantize_blocks(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
+                            block_ids=None, dev_status=None, stream=None) -> PreparedCall:
+    """``pkv_quantize_blocks`` with its arguments marshalled once."""
+    return PreparedCall(*_quantize("pkv_quantize_blocks", k_fp16, v_fp16, k_codes, v_codes,
+                                   k_scales, v_scales, block_ids, dev_status, stream),
+                        keep=(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, block_ids,
+                              dev_status))
+
+
+def prepare_quantize_blocks_fp8(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales,
+                                block_ids=None, dev_status=None, stream=None) -> PreparedCall:
+    """``pkv_quantize_blocks_fp8`` with its arguments marshalled once."""
+    return PreparedCall(*_quantize("pkv_quantize_blocks_fp8", k_fp16, v_fp16, k_codes, v_codes,
+                                   k_scales, v_scales, block_ids, dev_status, stream),
+                        keep=(k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, block_ids,
+                              dev_status))
 
 
 def _quantize(fn_name, k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, block_ids,
               dev_status, stream):
+    """Checks and marshals a quantize call: (C function name, arguments)."""
     import torch
     code_t = torch.uint8 if fn_name.endswith("fp8") else torch.int8
     _check(k_fp16, "k_fp16", torch.float16)
@@ -232,16 +290,14 @@ def _quantize(fn_name, k_fp16, v_fp16, k_codes, v_codes, k_scales, v_scales, blo
     _check(dev_status, "dev_status", torch.int32)
     nb, hkv, bs, d = k_fp16.shape
     nids = 0 if block_ids is None else block_ids.numel()
-    st = getattr(lib(), fn_name)(
-        _ptr(k_fp16), _ptr(v_fp16), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
-        _ptr(v_scales), _ptr(block_ids), nids, nb, hkv, d, bs, _ptr(dev_status),
-        _stream(stream))
-    if st != PKV_OK:
-        raise PkvError(st, fn_name)
+    return fn_name, [_ptr(k_fp16), _ptr(v_fp16), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+                     _ptr(v_scales), _ptr(block_ids), nids, nb, hkv, d, bs, _ptr(dev_status),
+                     _stream(stream)]
 
 
 def _decode(fn_name, out, query, kp, vp, ks, vs, block_tables, context_lens,
             max_context_len, softmax_scale, workspace, dev_status, stream):
+    """Checks and marshals a decode call: (C function name, arguments)."""
     import torch
     # the per-step inputs and the output may live in pinned host memory
     _check(out, "out", torch.float32, host_ok=True)
@@ -250,6 +306,15 @@ def _decode(fn_name, out, query, kp, vp, ks, vs, block_tables, context_lens,
     _check(context_lens, "context_lens", torch.int32, host_ok=True)
     _check(workspace, "workspace")
     _check(dev_status, "dev_status", torch.int32)
+    if ks is None:
+        _check(kp, "k_cache", torch.float16)
+        _check(vp, "v_cache", torch.float16)
+    else:
+        code_t = torch.uint8 if fn_name.endswith("fp8") else torch.int8
+        _check(kp, "k_codes", code_t)
+        _check(vp, "v_codes", code_t)
+        _check(ks, "k_scales", torch.float32)
+        _check(vs, "v_scales", torch.float32)
     n, hq, d = query.shape
     nb, hkv, bs, _ = kp.shape
     mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
@@ -260,48 +325,67 @@ def _decode(fn_name, out, query, kp, vp, ks, vs, block_tables, context_lens,
     args += [nb, _ptr(block_tables), mb, _ptr(context_lens), int(max_context_len), n, hq, hkv,
              d, bs, float(softmax_scale), _ptr(workspace), ws_bytes, _ptr(dev_status),
              _stream(stream)]
-    st = getattr(lib(), fn_name)(*args)
-    if st != PKV_OK:
-        raise PkvError(st, fn_name)
+    return fn_name, args
 
 
 def pkv_paged_decode_fp16(out, query, k_cache, v_cache, block_tables, context_lens,
                           max_context_len, softmax_scale, workspace, dev_status=None,
                           stream=None) -> None:
     """out[N][Hq][d] fp32 = decode attention of query over fp16 pools."""
-    import torch
-    _check(k_cache, "k_cache", torch.float16)
-    _check(v_cache, "v_cache", torch.float16)
-    _decode("pkv_paged_decode_fp16", out, query, k_cache, v_cache, None, None, block_tables,
-            context_lens, max_context_len, softmax_scale, workspace, dev_status, stream)
+    _invoke(*_decode("pkv_paged_decode_fp16", out, query, k_cache, v_cache, None, None,
+                     block_tables, context_lens, max_context_len, softmax_scale, workspace,
+                     dev_status, stream))
 
 
 def pkv_paged_decode_int8(out, query, k_codes, v_codes, k_scales, v_scales, block_tables,
                           context_lens, max_context_len, softmax_scale, workspace,
                           dev_status=None, stream=None) -> None:
     """out[N][Hq][d] fp32 = decode attention of query over INT8 pools + scales."""
-    import torch
-    _check(k_codes, "k_codes", torch.int8)
-    _check(v_codes, "v_codes", torch.int8)
-    _check(k_scales, "k_scales", torch.float32)
-    _check(v_scales, "v_scales", torch.float32)
-    _decode("pkv_paged_decode_int8", out, query, k_codes, v_codes, k_scales, v_scales,
-            block_tables, context_lens, max_context_len, softmax_scale, workspace, dev_status,
-            stream)
+    _invoke(*_decode("pkv_paged_decode_int8", out, query, k_codes, v_codes, k_scales, v_scales,
+                     block_tables, context_lens, max_context_len, softmax_scale, workspace,
+                     dev_status, stream))
 
 
 def pkv_paged_decode_fp8(out, query, k_codes, v_codes, k_scales, v_scales, block_tables,
                          context_lens, max_context_len, softmax_scale, workspace,
                          dev_status=None, stream=None) -> None:
     """out[N][Hq][d] fp32 = decode attention of query over FP8 (E4M3) pools."""
-    import torch
-    _check(k_codes, "k_codes", torch.uint8)
-    _check(v_codes, "v_codes", torch.uint8)
-    _check(k_scales, "k_scales", torch.float32)
-    _check(v_scales, "v_scales", torch.float32)
-    _decode("pkv_paged_decode_fp8", out, query, k_codes, v_codes, k_scales, v_scales,
-            block_tables, context_lens, max_context_len, softmax_scale, workspace, dev_status,
-            stream)
+    _invoke(*_decode("pkv_paged_decode_fp8", out, query, k_codes, v_codes, k_scales, v_scales,
+                     block_tables, context_lens, max_context_len, softmax_scale, workspace,
+                     dev_status, stream))
+
+
+def prepare_paged_decode_fp16(out, query, k_cache, v_cache, block_tables, context_lens,
+                              max_context_len, softmax_scale, workspace, dev_status=None,
+                              stream=None) -> PreparedCall:
+    """``pkv_paged_decode_fp16`` with its arguments marshalled once."""
+    return PreparedCall(*_decode("pkv_paged_decode_fp16", out, query, k_cache, v_cache, None,
+                                 None, block_tables, context_lens, max_context_len,
+                                 softmax_scale, workspace, dev_status, stream),
+                        keep=(out, query, k_cache, v_cache, block_tables, context_lens,
+                              workspace, dev_status))
+
+
+def prepare_paged_decode_int8(out, query, k_codes, v_codes, k_scales, v_scales, block_tables,
+                              context_lens, max_context_len, softmax_scale, workspace,
+                              dev_status=None, stream=None) -> PreparedCall:
+    """``pkv_paged_decode_int8`` with its arguments marshalled once."""
+    return PreparedCall(*_decode("pkv_paged_decode_int8", out, query, k_codes, v_codes,
+                                 k_scales, v_scales, block_tables, context_lens,
+                                 max_context_len, softmax_scale, workspace, dev_status, stream),
+                        keep=(out, query, k_codes, v_codes, k_scales, v_scales, block_tables,
+                              context_lens, workspace, dev_status))
+
+
+def prepare_paged_decode_fp8(out, query, k_codes, v_codes, k_scales, v_scales, block_tables,
+                             context_lens, max_context_len, softmax_scale, workspace,
+                             dev_status=None, stream=None) -> PreparedCall:
+    """``pkv_paged_decode_fp8`` with its arguments marshalled once."""
+    return PreparedCall(*_decode("pkv_paged_decode_fp8", out, query, k_codes, v_codes,
+                                 k_scales, v_scales, block_tables, context_lens,
+                                 max_context_len, softmax_scale, workspace, dev_status, stream),
+                        keep=(out, query, k_codes, v_codes, k_scales, v_scales, block_tables,
+                              context_lens, workspace, dev_status))
 
 
 def decode_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, device=None):
