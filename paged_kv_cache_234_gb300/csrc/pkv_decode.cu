@@ -322,20 +322,37 @@ struct PageCursor {
     int page;    // page (16-token block) within the sequence
     int npages;  // pages of the sequence
 
-    __device__ void seek(const DecodeArgs &p, const int32_t *prefix, int64_t x)
+    // All 32 lanes of a warp, with the same x.  The sequence is the largest s
+    // with items_per_seq * prefix[s] <= x (prefix is nondecreasing, so the
+    // s that pass form a run from 0): each round tests 32 evenly spaced
+    // candidates of the remaining range with one ballot and keeps the span
+    // after the last one that passes, down to 32 candidates, then counts.
+    // The item within the sequence is counted the same way when a sequence
+    // has at most 32 items.
+    __device__ void seek(const DecodeArgs &p, const int32_t *prefix, int64_t x, int lane)
     {
-        int lo = 0, hi = p.num_seqs;  // largest s with items_per_seq * prefix[s] <= x
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (static_cast<int64_t>(p.items_per_seq) * prefix[PKV_IDX(mid, p.num_seqs + 1)] <= x)
-                lo = mid;
-            else
-                hi = mid;
+        const int64_t ips = p.items_per_seq;
+        int lo = 0, span = p.num_seqs;  // prefix[lo] * ips <= x throughout
+        while (span > 32) {
+            const int step = (span + 31) >> 5;
+            const int sc = lo + lane * step;
+            const bool le = lane * step < span &&
+                            ips * prefix[PKV_IDX(sc, p.num_seqs + 1)] <= x;
+            const int c = __popc(__ballot_sync(0xffffffffu, le));
+            lo += (c - 1) * step;
+            span = min(step, span - (c - 1) * step);
         }
-        seq = lo;
-        npages = prefix[PKV_IDX(lo + 1, p.num_seqs + 1)] - prefix[lo];
-        const int64_t r = x - static_cast<int64_t>(p.items_per_seq) * prefix[lo];
-        if (r <= 0xffffffffll) {
+        {
+            const bool le = lane < span && ips * prefix[PKV_IDX(lo + lane, p.num_seqs + 1)] <= x;
+            seq = lo + __popc(__ballot_sync(0xffffffffu, le)) - 1;
+        }
+        npages = prefix[PKV_IDX(seq + 1, p.num_seqs + 1)] - prefix[seq];
+        const int64_t r = x - ips * prefix[seq];
+        if (ips <= 32) {
+            const bool le = lane < ips && static_cast<int64_t>(lane) * npages <= r;
+            item = __popc(__ballot_sync(0xffffffffu, le)) - 1;
+            page = static_cast<int>(r - static_cast<int64_t>(item) * npages);
+        } else if (r <= 0xffffffffll) {
             const uint32_t r32 = static_cast<uint32_t>(r);
             item = static_cast<int>(r32 / static_cast<uint32_t>(npages));
             page = static_cast<int>(r32 - static_cast<uint32_t>(item) * static_cast<uint32_t>(npages));
@@ -343,8 +360,13 @@ struct PageCursor {
             item = static_cast<int>(r / npages);
             page = static_cast<int>(r % npages);
         }
-        kvh = item / p.qgroups;
-        qg = item - kvh * p.qgroups;
+        if (p.qgroups == 1) {
+            kvh = item;
+            qg = 0;
+        } else {
+            kvh = item / p.qgroups;
+            qg = item - kvh * p.qgroups;
+        }
     }
 
     // pages of the next stage: up to pps, never past the item's end or `left`
@@ -672,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
         const int64_t b = muldiv(w + 1, total, p.num_workers);
         if (a >= b) return;
         n = static_cast<int>(b - a);
-        ci.seek(p, prefix, a);
+        ci.seek(p, prefix, a, lane);
     }
 
     const uint32_t stage0 = ptx::smem_addr(smem) + warp * S * C::kStageBytes;
