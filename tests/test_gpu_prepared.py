@@ -107,3 +107,26 @@ def test_prepared_call_reports_errors_when_called():
     with pytest.raises(pkv.PkvError) as e:
         call()
     assert e.value.status == pkv.PKV_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("case", ["cluster", "persistent"])
+def test_prepared_decode_with_host_resident_step_arguments(case):
+    # query, block tables, context lengths and output in pinned host memory,
+    # read and written in place by the kernels: the same bits as device tensors
+    ensure_built()
+    w = _case(case, 506)
+    n, hq, d = w.query.shape
+    mcl = w.max_context_len
+    codes = tuple(dev(x) for x in oracle_codes(w))
+    ws = pkv.decode_workspace(n, hq, w.num_kv_heads, d, mcl)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    q_h, bt_h, cl_h = pin(w.query), pin(w.block_tables), pin(w.context_lens)
+    out_h = torch.full((n, hq, d), float("nan"), dtype=torch.float32).pin_memory()
+    out_d = torch.full((n, hq, d), float("nan"), dtype=torch.float32, device="cuda")
+    host = pkv.prepare_paged_decode_int8(out_h, q_h, *codes, bt_h, cl_h, mcl, w.softmax_scale, ws)
+    devc = pkv.prepare_paged_decode_int8(out_d, dev(w.query), *codes, dev(w.block_tables),
+                                         dev(w.context_lens), mcl, w.softmax_scale, ws)
+    host()
+    devc()
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int32), out_d.cpu().view(torch.int32))
