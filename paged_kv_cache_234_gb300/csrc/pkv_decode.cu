@@ -89,9 +89,10 @@ struct DecodeArgs {
     int32_t *dev_status;
     int num_seqs, num_heads, num_kv_heads;
     int group;           // query heads per kv head
-    int qgroups;         // ceil(group / 8)
+    int item_heads;      // query heads per work item: 8, or 16 when group > 8
+    int qgroups;         // ceil(group / item_heads)
     int items_per_seq;   // num_kv_heads * qgroups
-    int rec_heads;       // min(8, group): heads per partial record
+    int rec_heads;       // min(item_heads, group): heads per partial record
     int max_blocks_per_seq;
     int num_blocks;
     int ctx_cap;         // largest valid context length
@@ -430,15 +431,21 @@ __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t total, int worke
     return static_cast<int64_t>(num / static_cast<uint64_t>(total));
 }
 
-// S^T fragment (rows: tokens g, g+8; cols: heads 2c, 2c+1) of one page.
-template <int kKv, int kD>
-__device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD / 16][2],
-                                            int lane, float (&s)[4])
+// S^T fragments (rows: tokens g, g+8; cols: heads 2c, 2c+1 of each of kG
+// groups of 8 query heads) of one page: every K fragment is loaded and
+// widened once and multiplied with each group's query fragments.
+template <int kKv, int kD, int kG>
+__device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kG][kD / 16][2],
+                                            int lane, float (&s)[kG][4])
 {
     using C = Cfg<kKv, kD>;
     constexpr bool kInt8 = C::kInt8;
     constexpr int KS = kD / 16;
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    float sa[kG][4], sb[kG][4];
+#pragma unroll
+    for (int gi = 0; gi < kG; ++gi)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sa[gi][i] = sb[gi][i] = 0.f;
     if constexpr (!kInt8) {
         const int lt = (lane & 7) + 8 * ((lane >> 3) & 1);
         const int lch = lane >> 4;
@@ -446,10 +453,13 @@ __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD
         for (int ks = 0; ks < KS; ++ks) {
             uint32_t a0, a1, a2, a3;
             ptx::ldsm_x4(PKV_SMEM(kt + swz<C::kRowBytes>(lt, 2 * ks + lch), 16, 16), a0, a1, a2, a3);
-            if (ks & 1)
-                ptx::mma_16816(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-            else
-                ptx::mma_16816(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+#pragma unroll
+            for (int gi = 0; gi < kG; ++gi) {
+                if (ks & 1)
+                    ptx::mma_16816(sb[gi], a0, a1, a2, a3, qf[gi][ks][0], qf[gi][ks][1]);
+                else
+                    ptx::mma_16816(sa[gi], a0, a1, a2, a3, qf[gi][ks][0], qf[gi][ks][1]);
+            }
         }
     } else {
         // lane (g, c): rows g and g+8, bytes [DG*c, DG*c + DG), DG = kD/4; the
@@ -485,14 +495,19 @@ __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD
                 a1 = ptx::e4m3x2_to_f16x2(kw[1][ks]);
                 a3 = ptx::e4m3x2_to_f16x2(kw[1][ks] >> 16);
             }
-            if (ks & 1)
-                ptx::mma_16816(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-            else
-                ptx::mma_16816(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+#pragma unroll
+            for (int gi = 0; gi < kG; ++gi) {
+                if (ks & 1)
+                    ptx::mma_16816(sb[gi], a0, a1, a2, a3, qf[gi][ks][0], qf[gi][ks][1]);
+                else
+                    ptx::mma_16816(sa[gi], a0, a1, a2, a3, qf[gi][ks][0], qf[gi][ks][1]);
+            }
         }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] = sa[i] + sb[i];
+    for (int gi = 0; gi < kG; ++gi)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[gi][i] = sa[gi][i] + sb[gi][i];
 }
 
 // O^T += V_page^T . P^T for one page; tokens >= ntok contribute nothing.
@@ -501,11 +516,13 @@ __device__ __forceinline__ void page_scores(uint32_t kt, const uint32_t (&qf)[kD
 // Otherwise P^T arrives as two f16 operands whose sum is the fp32
 // probabilities (high part pb0/pb1, low part pl0/pl1) and both products go
 // into the same fp32 accumulators.  Either way P is not rounded to f16
-// precision.
-template <int kKv, int kD, bool kLoCols>
-__device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1, uint32_t pl0,
-                                        uint32_t pl1, int ntok, int lane,
-                                        float (&o)[kD / 16][4])
+// precision.  Every V fragment is loaded and widened once and multiplied
+// with each of the kG groups' probabilities.
+template <int kKv, int kD, bool kLoCols, int kG>
+__device__ __forceinline__ void page_pv(uint32_t vt, const uint32_t (&pb0)[kG],
+                                        const uint32_t (&pb1)[kG], const uint32_t (&pl0)[kG],
+                                        const uint32_t (&pl1)[kG], int ntok, int lane,
+                                        float (&o)[kG][kD / 16][4])
 {
     using C = Cfg<kKv, kD>;
     constexpr bool kInt8 = C::kInt8;
@@ -527,8 +544,11 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
             a1 &= mlo;
             a2 &= mhi;
             a3 &= mhi;
-            ptx::mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
-            if constexpr (!kLoCols) ptx::mma_16816(o[i], a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+            for (int gi = 0; gi < kG; ++gi) {
+                ptx::mma_16816(o[gi][i], a0, a1, a2, a3, pb0[gi], pb1[gi]);
+                if constexpr (!kLoCols) ptx::mma_16816(o[gi][i], a0, a1, a2, a3, pl0[gi], pl1[gi]);
+            }
         }
     } else {
         // lane (g, c): tokens 2c, 2c+1, 2c+8, 2c+9; bytes [DG*g, DG*g + DG), DG = kD/8
@@ -575,8 +595,11 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
                 a2 = ptx::e4m3x2_to_f16x2(il23) & mhi;
                 a3 = ptx::e4m3x2_to_f16x2(il23 >> 16) & mhi;
             }
-            ptx::mma_16816(o[i], a0, a1, a2, a3, pb0, pb1);
-            if constexpr (!kLoCols) ptx::mma_16816(o[i], a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+            for (int gi = 0; gi < kG; ++gi) {
+                ptx::mma_16816(o[gi][i], a0, a1, a2, a3, pb0[gi], pb1[gi]);
+                if constexpr (!kLoCols) ptx::mma_16816(o[gi][i], a0, a1, a2, a3, pl0[gi], pl1[gi]);
+            }
         }
     }
 }
@@ -589,12 +612,14 @@ __device__ __forceinline__ void page_pv(uint32_t vt, uint32_t pb0, uint32_t pb1,
 // eight columns and a second PV mma for the low parts.
 // kClust: one item per thread-block cluster of p.clust CTAs (small batches);
 // otherwise persistent workers over the whole page stream.
-template <int kKv, int kD, bool kLoCols, bool kClust>
-__global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
+template <int kKv, int kD, bool kLoCols, bool kClust, int kG>
+__global__ void __launch_bounds__(kThreads, kG == 1 ? Cfg<kKv, kD>::kMinCtas : (kD == 128 ? 2 : 3))
     decode_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv)
 {
     using C = Cfg<kKv, kD>;
+    static_assert(kG == 1 || !kLoCols, "several groups per item use all eight mma columns");
+    constexpr int kGH = kItemHeads * kG;  // query heads per work item
     constexpr bool kInt8 = C::kInt8;
     constexpr int S = C::kStages;
     constexpr int PPS = C::kPPS;
@@ -783,12 +808,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     if (ipos < n && lane < ci.unit(PPS, n - ipos))
         nblk = __ldg(PKV_TABLE_AT(p, ci.seq, ci.page, lane, mb));
 
-    // ---- per-piece state
-    float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 units), heads 2c and 2c+1
-    float l0 = 0.f, l1 = 0.f;              // lane-partial running sums
-    float o[KS][4];                        // O^T accumulators (see the output mapping)
-    uint32_t qf[KS][2];                    // Q^T B-fragments
-    float qb0 = 0.f, qb1 = 0.f;            // INT8: 1152 * sum(q) of heads 2c, 2c+1
+    // ---- per-piece state, per group of 8 query heads (the item's kG groups
+    // share every page)
+    float m0[kG], m1[kG];    // running max (log2 units), heads 2c and 2c+1 of the group
+    float l0[kG], l1[kG];    // lane-partial running sums
+    float o[kG][KS][4];      // O^T accumulators (see the output mapping)
+    uint32_t qf[kG][KS][2];  // Q^T B-fragments
+    float qb0[kG], qb1[kG];  // INT8: 1152 * sum(q) of heads 2c, 2c+1
+#pragma unroll
+    for (int gi = 0; gi < kG; ++gi) {
+        m0[gi] = m1[gi] = -INFINITY;
+        l0[gi] = l1[gi] = 0.f;
+        qb0[gi] = qb1[gi] = 0.f;
+    }
     // Codes: V scale reference of the piece (the largest V scale of its pages
     // so far) and its reciprocal.  A page enters PV with its probabilities
     // times sv / vref <= 1, so the f16 operand keeps its full precision
@@ -808,55 +840,65 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
         const int cnt = cc.unit(PPS, n - pos);
         const bool first = pos == 0 || cc.page == 0;
         const bool last = pos + cnt == n || cc.page + cnt == cc.npages;
-        const int h0 = cc.kvh * p.group + cc.qg * kItemHeads;
-        const int gh = min(kItemHeads, p.group - cc.qg * kItemHeads);
+        const int h0 = cc.kvh * p.group + cc.qg * kGH;
+        const int gh = min(kGH, p.group - cc.qg * kGH);
 
         if (first) {
-            // query fragments of the item's heads (column g: head g, or head
-            // g mod 4 with kLoCols); heads past gh are zero
-            const int hq = kLoCols ? (g & 3) : g;
-            const __half *qrow =
-                p.query + (static_cast<int64_t>(cc.seq) * p.num_heads + h0 + hq) * kD;
-            const bool live = hq < gh;
-            if constexpr (kInt8) {
-                // lane (g, c) holds q[g][DG*c .. DG*c + DG), DG = kD / 4
-                constexpr int DG = kD / 4;
-                uint4 qv[DG / 8];
+            // query fragments of the item's heads (group gi, column g: head
+            // 8 gi + g, or g mod 4 with kLoCols); heads past gh are zero
 #pragma unroll
-                for (int j = 0; j < DG / 8; ++j)
-                    qv[j] = live ? __ldg(reinterpret_cast<const uint4 *>(qrow + DG * c) + j)
-                                 : make_uint4(0, 0, 0, 0);
-                const uint32_t *qw = reinterpret_cast<const uint32_t *>(qv);
-                float qs = 0.f;
+            for (int gi = 0; gi < kG; ++gi) {
+                const int hq = kItemHeads * gi + (kLoCols ? (g & 3) : g);
+                const __half *qrow =
+                    p.query + (static_cast<int64_t>(cc.seq) * p.num_heads + h0 + hq) * kD;
+                const bool live = hq < gh;
+                if constexpr (kInt8) {
+                    // lane (g, c) holds q[g][DG*c .. DG*c + DG), DG = kD / 4
+                    constexpr int DG = kD / 4;
+                    uint4 qv[DG / 8];
 #pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    qf[s][0] = qw[2 * s];
-                    qf[s][1] = qw[2 * s + 1];
-                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&qw[2 * s]));
-                    const float2 f1 =
-                        __half22float2(*reinterpret_cast<const __half2 *>(&qw[2 * s + 1]));
-                    qs += (f0.x + f0.y) + (f1.x + f1.y);
-                }
-                // sum over the head's four lanes, then fetch heads 2c and 2c+1
-                qs += __shfl_xor_sync(0xffffffffu, qs, 1);
-                qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-                if constexpr (kKv == kKvI8) {  // FP8 codes carry no bias
-                    qb0 = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c);
-                    qb1 = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
-                }
-            } else {
-                const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
+                    for (int j = 0; j < DG / 8; ++j)
+                        qv[j] = live ? __ldg(reinterpret_cast<const uint4 *>(qrow + DG * c) + j)
+                                     : make_uint4(0, 0, 0, 0);
+                    const uint32_t *qw = reinterpret_cast<const uint32_t *>(qv);
+                    float qs = 0.f;
 #pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    qf[s][0] = live ? __ldg(qw + 8 * s + c) : 0u;
-                    qf[s][1] = live ? __ldg(qw + 8 * s + 4 + c) : 0u;
+                    for (int s = 0; s < KS; ++s) {
+                        qf[gi][s][0] = qw[2 * s];
+                        qf[gi][s][1] = qw[2 * s + 1];
+                        const float2 f0 =
+                            __half22float2(*reinterpret_cast<const __half2 *>(&qw[2 * s]));
+                        const float2 f1 =
+                            __half22float2(*reinterpret_cast<const __half2 *>(&qw[2 * s + 1]));
+                        qs += (f0.x + f0.y) + (f1.x + f1.y);
+                    }
+                    // sum over the head's four lanes, then fetch heads 2c and 2c+1
+                    qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+                    qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+                    if constexpr (kKv == kKvI8) {  // FP8 codes carry no bias
+                        qb0[gi] = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c);
+                        qb1[gi] = 1152.f * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
+                    }
+                } else {
+                    const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
+#pragma unroll
+                    for (int s = 0; s < KS; ++s) {
+                        qf[gi][s][0] = live ? __ldg(qw + 8 * s + c) : 0u;
+                        qf[gi][s][1] = live ? __ldg(qw + 8 * s + 4 + c) : 0u;
+                    }
                 }
             }
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < kG; ++gi) {
+                m0[gi] = m1[gi] = -INFINITY;
+                l0[gi] = l1[gi] = 0.f;
+            }
             vref = vinv = 0.f;
 #pragma unroll
-            for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            for (int gi = 0; gi < kG; ++gi)
+#pragma unroll
+                for (int i = 0; i < KS; ++i)
+                    o[gi][i][0] = o[gi][i][1] = o[gi][i][2] = o[gi][i][3] = 0.f;
             piece_bad = false;
             piece_has_a = pos == 0;
             piece_first_page = cc.page;
@@ -896,51 +938,67 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
             const uint32_t st = stage0 + slot * C::kStageBytes;
             const int ctx = kClust ? cctx : ctxs[PKV_IDX(cc.seq, p.num_seqs)];
             // ---- scores of the stage's pages, base-2 logits
-            float x[PPS][4];
+            float x[kG][PPS][4];
 #pragma unroll
             for (int u = 0; u < PPS; ++u) {
                 if (good[u]) {
-                    float sc[4];
-                    page_scores<kKv, kD>(st + u * C::kPageBytes, qf, lane, sc);
+                    float sc[kG][4];
+                    page_scores<kKv, kD, kG>(st + u * C::kPageBytes, qf, lane, sc);
                     float sl = p.scale_log2;
-                    if constexpr (kInt8) {
-                        sl *= hf[2 + u];
-                        x[u][0] = (sc[0] - qb0) * sl;
-                        x[u][1] = (sc[1] - qb1) * sl;
-                        x[u][2] = (sc[2] - qb0) * sl;
-                        x[u][3] = (sc[3] - qb1) * sl;
-                    } else {
-                        x[u][0] = sc[0] * sl;
-                        x[u][1] = sc[1] * sl;
-                        x[u][2] = sc[2] * sl;
-                        x[u][3] = sc[3] * sl;
-                    }
+                    if constexpr (kInt8) sl *= hf[2 + u];
                     const int ntok = ctx - (cc.page + u) * kPage;
-                    if (ntok < kPage) {
-                        if (g >= ntok) x[u][0] = x[u][1] = -INFINITY;
-                        if (g + 8 >= ntok) x[u][2] = x[u][3] = -INFINITY;
+#pragma unroll
+                    for (int gi = 0; gi < kG; ++gi) {
+                        if constexpr (kInt8) {
+                            x[gi][u][0] = (sc[gi][0] - qb0[gi]) * sl;
+                            x[gi][u][1] = (sc[gi][1] - qb1[gi]) * sl;
+                            x[gi][u][2] = (sc[gi][2] - qb0[gi]) * sl;
+                            x[gi][u][3] = (sc[gi][3] - qb1[gi]) * sl;
+                        } else {
+                            x[gi][u][0] = sc[gi][0] * sl;
+                            x[gi][u][1] = sc[gi][1] * sl;
+                            x[gi][u][2] = sc[gi][2] * sl;
+                            x[gi][u][3] = sc[gi][3] * sl;
+                        }
+                        if (ntok < kPage) {
+                            if (g >= ntok) x[gi][u][0] = x[gi][u][1] = -INFINITY;
+                            if (g + 8 >= ntok) x[gi][u][2] = x[gi][u][3] = -INFINITY;
+                        }
                     }
                 } else {
-                    x[u][0] = x[u][1] = x[u][2] = x[u][3] = -INFINITY;
+#pragma unroll
+                    for (int gi = 0; gi < kG; ++gi)
+                        x[gi][u][0] = x[gi][u][1] = x[gi][u][2] = x[gi][u][3] = -INFINITY;
                 }
             }
-            // ---- online softmax, one update for the whole stage
-            float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+            // ---- online softmax, one update for the whole stage, per group
+            float mn0[kG], mn1[kG], al0[kG], al1[kG];
 #pragma unroll
-            for (int u = 1; u < PPS; ++u) {
-                mx0 = fmaxf(mx0, fmaxf(x[u][0], x[u][2]));
-                mx1 = fmaxf(mx1, fmaxf(x[u][1], x[u][3]));
-            }
+            for (int gi = 0; gi < kG; ++gi) {
+                float mx0 = fmaxf(x[gi][0][0], x[gi][0][2]), mx1 = fmaxf(x[gi][0][1], x[gi][0][3]);
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                for (int u = 1; u < PPS; ++u) {
+                    mx0 = fmaxf(mx0, fmaxf(x[gi][u][0], x[gi][u][2]));
+                    mx1 = fmaxf(mx1, fmaxf(x[gi][u][1], x[gi][u][3]));
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                mn0[gi] = fmaxf(m0[gi], mx0);
+                mn1[gi] = fmaxf(m1[gi], mx1);
+                al0[gi] = ptx::ex2(m0[gi] - mn0[gi]);
+                al1[gi] = ptx::ex2(m1[gi] - mn1[gi]);
+                m0[gi] = mn0[gi];
+                m1[gi] = mn1[gi];
             }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float al0 = ptx::ex2(m0 - mn0), al1 = ptx::ex2(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            float oa0 = al0, oa1 = al1;  // rescale of the accumulators
+            float oa0[kG], oa1[kG];  // rescale of the accumulators
+#pragma unroll
+            for (int gi = 0; gi < kG; ++gi) {
+                oa0[gi] = al0[gi];
+                oa1[gi] = al1[gi];
+            }
             [[maybe_unused]] float vr[PPS];
             if constexpr (kInt8) {
                 // a page with a larger V scale becomes the reference: the
@@ -953,33 +1011,39 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
                     vinv = __frcp_rn(smax);
                     const float ratio = vref * vinv;
                     vinv *= kPScale;
-                    oa0 *= ratio;
-                    oa1 *= ratio;
+#pragma unroll
+                    for (int gi = 0; gi < kG; ++gi) {
+                        oa0[gi] *= ratio;
+                        oa1[gi] *= ratio;
+                    }
                     vref = smax;
                 }
 #pragma unroll
                 for (int u = 0; u < PPS; ++u) vr[u] = hf[4 + u] * vinv;
             }
-            float pr[PPS][4];
-            float ps0 = 0.f, ps1 = 0.f;
+            float pr[kG][PPS][4];
 #pragma unroll
-            for (int u = 0; u < PPS; ++u) {
-                pr[u][0] = ptx::ex2(x[u][0] - mn0);
-                pr[u][1] = ptx::ex2(x[u][1] - mn1);
-                pr[u][2] = ptx::ex2(x[u][2] - mn0);
-                pr[u][3] = ptx::ex2(x[u][3] - mn1);
-                ps0 += pr[u][0] + pr[u][2];
-                ps1 += pr[u][1] + pr[u][3];
-            }
-            l0 = l0 * al0 + ps0;
-            l1 = l1 * al1 + ps1;
-            if (__any_sync(0xffffffffu, oa0 != 1.f || oa1 != 1.f)) {
+            for (int gi = 0; gi < kG; ++gi) {
+                float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-                for (int i = 0; i < KS; ++i) {
-                    o[i][0] *= oa0;
-                    o[i][1] *= oa1;
-                    o[i][2] *= oa0;
-                    o[i][3] *= oa1;
+                for (int u = 0; u < PPS; ++u) {
+                    pr[gi][u][0] = ptx::ex2(x[gi][u][0] - mn0[gi]);
+                    pr[gi][u][1] = ptx::ex2(x[gi][u][1] - mn1[gi]);
+                    pr[gi][u][2] = ptx::ex2(x[gi][u][2] - mn0[gi]);
+                    pr[gi][u][3] = ptx::ex2(x[gi][u][3] - mn1[gi]);
+                    ps0 += pr[gi][u][0] + pr[gi][u][2];
+                    ps1 += pr[gi][u][1] + pr[gi][u][3];
+                }
+                l0[gi] = l0[gi] * al0[gi] + ps0;
+                l1[gi] = l1[gi] * al1[gi] + ps1;
+                if (__any_sync(0xffffffffu, oa0[gi] != 1.f || oa1[gi] != 1.f)) {
+#pragma unroll
+                    for (int i = 0; i < KS; ++i) {
+                        o[gi][i][0] *= oa0[gi];
+                        o[gi][i][1] *= oa1[gi];
+                        o[gi][i][2] *= oa0[gi];
+                        o[gi][i][3] *= oa1[gi];
+                    }
                 }
             }
             // ---- O^T += V^T . P^T per page (P^T: transposed 8x8 halves of P)
@@ -991,26 +1055,30 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
                     // number down to p = 2^-29 and the low part adds the
                     // next 11 bits
                     const float sc = kInt8 ? vr[u] : kPScale;
-                    const float pa = pr[u][0] * sc, pb = pr[u][1] * sc;
-                    const float pc = pr[u][2] * sc, pd = pr[u][3] * sc;
-                    const uint32_t h01 = pack_half2(pa, pb), h23 = pack_half2(pc, pd);
-                    const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
-                    uint32_t pb0, pb1, pl0 = 0, pl1 = 0;
-                    if constexpr (kLoCols) {
-                        // columns 0-3 (c < 2): high parts; 4-7: low parts
-                        pb0 = ptx::movmatrix_t(
-                            pack_half2(fmaf(-lo_sel, f01.x, pa), fmaf(-lo_sel, f01.y, pb)));
-                        pb1 = ptx::movmatrix_t(
-                            pack_half2(fmaf(-lo_sel, f23.x, pc), fmaf(-lo_sel, f23.y, pd)));
-                    } else {
-                        pb0 = ptx::movmatrix_t(h01);
-                        pb1 = ptx::movmatrix_t(h23);
-                        pl0 = ptx::movmatrix_t(pack_half2(pa - f01.x, pb - f01.y));
-                        pl1 = ptx::movmatrix_t(pack_half2(pc - f23.x, pd - f23.y));
+                    uint32_t pb0[kG], pb1[kG], pl0[kG], pl1[kG];
+#pragma unroll
+                    for (int gi = 0; gi < kG; ++gi) {
+                        const float pa = pr[gi][u][0] * sc, pb = pr[gi][u][1] * sc;
+                        const float pc = pr[gi][u][2] * sc, pd = pr[gi][u][3] * sc;
+                        const uint32_t h01 = pack_half2(pa, pb), h23 = pack_half2(pc, pd);
+                        const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
+                        pl0[gi] = pl1[gi] = 0;
+                        if constexpr (kLoCols) {
+                            // columns 0-3 (c < 2): high parts; 4-7: low parts
+                            pb0[gi] = ptx::movmatrix_t(
+                                pack_half2(fmaf(-lo_sel, f01.x, pa), fmaf(-lo_sel, f01.y, pb)));
+                            pb1[gi] = ptx::movmatrix_t(
+                                pack_half2(fmaf(-lo_sel, f23.x, pc), fmaf(-lo_sel, f23.y, pd)));
+                        } else {
+                            pb0[gi] = ptx::movmatrix_t(h01);
+                            pb1[gi] = ptx::movmatrix_t(h23);
+                            pl0[gi] = ptx::movmatrix_t(pack_half2(pa - f01.x, pb - f01.y));
+                            pl1[gi] = ptx::movmatrix_t(pack_half2(pc - f23.x, pd - f23.y));
+                        }
                     }
                     const int ntok = min(kPage, ctx - (cc.page + u) * kPage);
-                    page_pv<kKv, kD, kLoCols>(st + u * C::kPageBytes + C::kTileBytes, pb0, pb1,
-                                              pl0, pl1, ntok, lane, o);
+                    page_pv<kKv, kD, kLoCols, kG>(st + u * C::kPageBytes + C::kTileBytes, pb0,
+                                                  pb1, pl0, pl1, ntok, lane, o);
                 }
             }
         }
@@ -1035,82 +1103,87 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
 
         // ---- piece finished: final output, or a partial for the reduce
         if (last) {
-            if constexpr (kLoCols) {
-                // add the low-part columns (lanes c + 2) to the high-part ones
-#pragma unroll
-                for (int i = 0; i < KS; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) o[i][j] += __shfl_xor_sync(0xffffffffu, o[i][j], 2);
-            }
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-            }
             const bool whole =
                 !kClust && piece_first_page == 0 && cc.page + cnt == cc.npages;
-            const int hA = 2 * c, hB = 2 * c + 1;
-            float *dstA, *dstB;
-            float fA, fB;
-            if (whole) {
-                const int64_t orow = (static_cast<int64_t>(cc.seq) * p.num_heads + h0) * kD;
-                dstA = p.out + orow + static_cast<int64_t>(hA) * kD;
-                dstB = p.out + orow + static_cast<int64_t>(hB) * kD;
-                const float vs = (kInt8 ? vref : 1.f) * kPScaleInv;
-                fA = piece_bad ? 0.f : vs / l0;
-                fB = piece_bad ? 0.f : vs / l1;
-            } else {
-                if constexpr (kClust) {
-                    // pushed to the shared memory of the CTAs merging hA, hB
-                    dstA = hA < gh ? crec_of(hA) + 4 : nullptr;
-                    dstB = hB < gh ? crec_of(hB) + 4 : nullptr;
+#pragma unroll
+            for (int gi = 0; gi < kG; ++gi) {
+                if constexpr (kLoCols) {
+                    // add the low-part columns (lanes c + 2) to the high-part ones
+#pragma unroll
+                    for (int i = 0; i < KS; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            o[gi][i][j] += __shfl_xor_sync(0xffffffffu, o[gi][i][j], 2);
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    l0[gi] += __shfl_xor_sync(0xffffffffu, l0[gi], off);
+                    l1[gi] += __shfl_xor_sync(0xffffffffu, l1[gi], off);
+                }
+                const int hA = kItemHeads * gi + 2 * c, hB = hA + 1;  // heads of the item
+                float *dstA, *dstB;
+                float fA, fB;
+                if (whole) {
+                    const int64_t orow = (static_cast<int64_t>(cc.seq) * p.num_heads + h0) * kD;
+                    dstA = p.out + orow + static_cast<int64_t>(hA) * kD;
+                    dstB = p.out + orow + static_cast<int64_t>(hB) * kD;
+                    const float vs = (kInt8 ? vref : 1.f) * kPScaleInv;
+                    fA = piece_bad ? 0.f : vs / l0[gi];
+                    fB = piece_bad ? 0.f : vs / l1[gi];
                 } else {
-                    const int slotp = piece_has_a ? 0 : 1;
-                    float *rec = p.partials + (static_cast<int64_t>(w) * 2 + slotp) *
-                                                  p.rec_heads * (kD + 4);
-                    dstA = rec + hA * (kD + 4) + 4;
-                    dstB = rec + hB * (kD + 4) + 4;
-                }
-                fA = fB = (kInt8 ? vref : 1.f) * kPScaleInv;  // accumulators in V units
-                if (g == 0) {
-                    if (hA < gh) {
-                        dstA[-4] = m0;
-                        dstA[-3] = piece_bad ? -1.f : l0;
+                    if constexpr (kClust) {
+                        // pushed to the shared memory of the CTAs merging hA, hB
+                        dstA = hA < gh ? crec_of(hA) + 4 : nullptr;
+                        dstB = hB < gh ? crec_of(hB) + 4 : nullptr;
+                    } else {
+                        const int slotp = piece_has_a ? 0 : 1;
+                        float *rec = p.partials + (static_cast<int64_t>(w) * 2 + slotp) *
+                                                      p.rec_heads * (kD + 4);
+                        dstA = rec + hA * (kD + 4) + 4;
+                        dstB = rec + hB * (kD + 4) + 4;
                     }
-                    if (hB < gh) {
-                        dstB[-4] = m1;
-                        dstB[-3] = piece_bad ? -1.f : l1;
-                    }
-                }
-            }
-            if (piece_bad) {
-#pragma unroll
-                for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-            }
-            if constexpr (!kInt8) {
-#pragma unroll
-                for (int i = 0; i < KS; ++i) {
-                    if (hA < gh) {
-                        dstA[16 * i + g] = o[i][0] * fA;
-                        dstA[16 * i + 8 + g] = o[i][2] * fA;
-                    }
-                    if (hB < gh) {
-                        dstB[16 * i + g] = o[i][1] * fB;
-                        dstB[16 * i + 8 + g] = o[i][3] * fB;
+                    fA = fB = (kInt8 ? vref : 1.f) * kPScaleInv;  // accumulators in V units
+                    if (g == 0) {
+                        if (hA < gh) {
+                            dstA[-4] = m0[gi];
+                            dstA[-3] = piece_bad ? -1.f : l0[gi];
+                        }
+                        if (hB < gh) {
+                            dstB[-4] = m1[gi];
+                            dstB[-3] = piece_bad ? -1.f : l1[gi];
+                        }
                     }
                 }
-            } else {
-                constexpr int DG = kD / 8;  // lane (g, c) owns d in [DG*g, DG*g + DG)
+                if (piece_bad) {
 #pragma unroll
-                for (int i = 0; i < KS; i += 2) {
-                    if (hA < gh)
-                        *reinterpret_cast<float4 *>(dstA + DG * g + 2 * i) =
-                            make_float4(o[i][0] * fA, o[i][2] * fA, o[i + 1][0] * fA,
-                                        o[i + 1][2] * fA);
-                    if (hB < gh)
-                        *reinterpret_cast<float4 *>(dstB + DG * g + 2 * i) =
-                            make_float4(o[i][1] * fB, o[i][3] * fB, o[i + 1][1] * fB,
-                                        o[i + 1][3] * fB);
+                    for (int i = 0; i < KS; ++i)
+                        o[gi][i][0] = o[gi][i][1] = o[gi][i][2] = o[gi][i][3] = 0.f;
+                }
+                if constexpr (!kInt8) {
+#pragma unroll
+                    for (int i = 0; i < KS; ++i) {
+                        if (hA < gh) {
+                            dstA[16 * i + g] = o[gi][i][0] * fA;
+                            dstA[16 * i + 8 + g] = o[gi][i][2] * fA;
+                        }
+                        if (hB < gh) {
+                            dstB[16 * i + g] = o[gi][i][1] * fB;
+                            dstB[16 * i + 8 + g] = o[gi][i][3] * fB;
+                        }
+                    }
+                } else {
+                    constexpr int DG = kD / 8;  // lane (g, c) owns d in [DG*g, DG*g + DG)
+#pragma unroll
+                    for (int i = 0; i < KS; i += 2) {
+                        if (hA < gh)
+                            *reinterpret_cast<float4 *>(dstA + DG * g + 2 * i) =
+                                make_float4(o[gi][i][0] * fA, o[gi][i][2] * fA,
+                                            o[gi][i + 1][0] * fA, o[gi][i + 1][2] * fA);
+                        if (hB < gh)
+                            *reinterpret_cast<float4 *>(dstB + DG * g + 2 * i) =
+                                make_float4(o[gi][i][1] * fB, o[gi][i][3] * fB,
+                                            o[gi][i + 1][1] * fB, o[gi][i + 1][3] * fB);
+                    }
                 }
             }
         }
@@ -1130,8 +1203,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kKv, kD>::kMinCtas)
     const int gi = blockIdx.x / p.clust;
     const int seq = gi / p.items_per_seq, item = gi - seq * p.items_per_seq;
     const int kvh = item / p.qgroups, qg = item - kvh * p.qgroups;
-    const int gh = min(kItemHeads, p.group - qg * kItemHeads);
-    const int h0 = kvh * p.group + qg * kItemHeads;
+    const int gh = min(kGH, p.group - qg * kGH);
+    const int h0 = kvh * p.group + qg * kGH;
     if (timed_out && lane < gh) crec_of(lane)[1] = -1.f;
     __syncwarp();
     ptx::cluster_sync();
@@ -1222,7 +1295,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const DecodeArgs p)
         const int item = rem / p.rec_heads;
         const int h = rem - item * p.rec_heads;
         const int kvh = item / p.qgroups, qg = item - kvh * p.qgroups;
-        const int gh = min(kItemHeads, p.group - qg * kItemHeads);
+        const int gh = min(p.item_heads, p.group - qg * p.item_heads);
         const int npages = prefix[seq + 1] - prefix[seq];
         if (h >= gh || npages == 0) continue;
         const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[seq] +
@@ -1329,7 +1402,7 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const DecodeArgs p)
                 }
             }
         }
-        const int h0 = kvh * p.group + qg * kItemHeads;
+        const int h0 = kvh * p.group + qg * p.item_heads;
         float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
         const float inv = bad ? 0.f : 1.f / L;
 #pragma unroll
@@ -1407,7 +1480,7 @@ struct DecodeCall {
 };
 
 struct Shape {
-    int group, qgroups, items_per_seq, rec_heads, ctx_cap;
+    int group, item_heads, qgroups, items_per_seq, rec_heads, ctx_cap;
     int64_t max_pages;  // upper bound of the page stream length
 };
 
@@ -1420,11 +1493,14 @@ pkv_status check_shape(int num_seqs, int num_heads, int num_kv_heads, int head_d
     if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     sh->group = num_heads / num_kv_heads;
-    sh->qgroups = (sh->group + kItemHeads - 1) / kItemHeads;
+    // a work item serves 8 query heads, or 16 (two groups of 8 sharing every
+    // staged page) when a kv head has more than 8
+    sh->item_heads = sh->group > kItemHeads ? 2 * kItemHeads : kItemHeads;
+    sh->qgroups = (sh->group + sh->item_heads - 1) / sh->item_heads;
     const int64_t ips = static_cast<int64_t>(num_kv_heads) * sh->qgroups;
     if (ips > (1 << 20)) return PKV_ERR_UNSUPPORTED;
     sh->items_per_seq = static_cast<int>(ips);
-    sh->rec_heads = sh->group < kItemHeads ? sh->group : kItemHeads;
+    sh->rec_heads = sh->group < sh->item_heads ? sh->group : sh->item_heads;
     const int64_t cap_tab = static_cast<int64_t>(max_blocks_per_seq) * kPage;
     sh->ctx_cap = static_cast<int>(max_context_len < cap_tab ? max_context_len : cap_tab);
     const int64_t pages_per_seq = (sh->ctx_cap + kPage - 1) / kPage;
@@ -1455,7 +1531,7 @@ struct ClusterCache {
     int clusters = 0;
 };
 
-template <int kKv, int kD, bool kLoCols>
+template <int kKv, int kD, bool kLoCols, int kG>
 pkv_status launch(const DecodeCall &call, const Shape &sh)
 {
     using C = Cfg<kKv, kD>;
@@ -1463,8 +1539,8 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     if (!current_device_info(&di)) return PKV_ERR_CUDA;
     const size_t smem = C::smem_bytes(call.num_seqs);
     if (smem > di.max_smem_optin) return PKV_ERR_UNSUPPORTED;
-    auto kern = decode_kernel<kKv, kD, kLoCols, false>;
-    auto kern_cl = decode_kernel<kKv, kD, kLoCols, true>;
+    auto kern = decode_kernel<kKv, kD, kLoCols, false, kG>;
+    auto kern_cl = decode_kernel<kKv, kD, kLoCols, true, kG>;
     static OccCache occ[64];
     static size_t smem_attr[2][64] = {};  // dynamic shared memory each kernel may use, per device
     static ClusterCache ccache[8];
@@ -1571,6 +1647,7 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     args.num_heads = call.num_heads;
     args.num_kv_heads = call.num_kv_heads;
     args.group = sh.group;
+    args.item_heads = sh.item_heads;
     args.qgroups = sh.qgroups;
     args.items_per_seq = sh.items_per_seq;
     args.rec_heads = sh.rec_heads;
@@ -1672,21 +1749,31 @@ pkv_status decode_entry(const DecodeCall &call, int kv)
     if (need > 0 && (!call.workspace || call.workspace_bytes < need)) return PKV_ERR_WORKSPACE;
     if (call.workspace && !aligned(call.workspace, 16)) return PKV_ERR_MISALIGNED;
     // groups of at most four query heads carry the low parts of the
-    // probabilities in the spare mma columns
-    const bool lo_cols = sh.group <= 4;
+    // probabilities in the spare mma columns; above eight, a work item
+    // serves two groups of eight from every staged page
+    const int variant = sh.group <= 4 ? 0 : sh.item_heads > kItemHeads ? 2 : 1;
+    auto pick = [&](auto lo, auto mid, auto two) -> pkv_status {
+        return variant == 0 ? lo(call, sh) : variant == 1 ? mid(call, sh) : two(call, sh);
+    };
     if (kv == kKvF8) {
         if (call.head_dim == 128)
-            return lo_cols ? launch<kKvF8, 128, true>(call, sh) : launch<kKvF8, 128, false>(call, sh);
-        return lo_cols ? launch<kKvF8, 64, true>(call, sh) : launch<kKvF8, 64, false>(call, sh);
+            return pick(launch<kKvF8, 128, true, 1>, launch<kKvF8, 128, false, 1>,
+                        launch<kKvF8, 128, false, 2>);
+        return pick(launch<kKvF8, 64, true, 1>, launch<kKvF8, 64, false, 1>,
+                    launch<kKvF8, 64, false, 2>);
     }
     if (kv == kKvI8) {
         if (call.head_dim == 128)
-            return lo_cols ? launch<kKvI8, 128, true>(call, sh) : launch<kKvI8, 128, false>(call, sh);
-        return lo_cols ? launch<kKvI8, 64, true>(call, sh) : launch<kKvI8, 64, false>(call, sh);
+            return pick(launch<kKvI8, 128, true, 1>, launch<kKvI8, 128, false, 1>,
+                        launch<kKvI8, 128, false, 2>);
+        return pick(launch<kKvI8, 64, true, 1>, launch<kKvI8, 64, false, 1>,
+                    launch<kKvI8, 64, false, 2>);
     }
     if (call.head_dim == 128)
-        return lo_cols ? launch<kKvF16, 128, true>(call, sh) : launch<kKvF16, 128, false>(call, sh);
-    return lo_cols ? launch<kKvF16, 64, true>(call, sh) : launch<kKvF16, 64, false>(call, sh);
+        return pick(launch<kKvF16, 128, true, 1>, launch<kKvF16, 128, false, 1>,
+                    launch<kKvF16, 128, false, 2>);
+    return pick(launch<kKvF16, 64, true, 1>, launch<kKvF16, 64, false, 1>,
+                launch<kKvF16, 64, false, 2>);
 }
 
 }  // namespace

@@ -48,14 +48,16 @@ def test_status_strings(L):
 
 
 def test_workspace_size_arithmetic(L):
-    # per worker: two partial records of min(8, group) heads x (d + 4) floats;
-    # at most 4096 workers and never more than the pages.
+    # per worker: two partial records of min(item heads, group) heads x
+    # (d + 4) floats, an item holding 8 query heads, or 16 when a kv head has
+    # more than 8; at most 4096 workers and never more than the pages.
     def expect(workers, heads, d):
         return workers * 2 * heads * (d + 4) * 4
     assert pkv.pkv_decode_workspace_size(64, 32, 8, 128, 2048) == expect(4096, 4, 128)
     assert pkv.pkv_decode_workspace_size(2, 8, 2, 64, 37) == expect(2 * 2 * 3, 4, 64)
     assert pkv.pkv_decode_workspace_size(8, 8, 8, 128, 512) == expect(2048, 1, 128)
-    assert pkv.pkv_decode_workspace_size(1, 32, 1, 128, 16) == expect(4, 8, 128)
+    assert pkv.pkv_decode_workspace_size(1, 32, 1, 128, 16) == expect(2, 16, 128)
+    assert pkv.pkv_decode_workspace_size(3, 12, 1, 64, 16) == expect(3, 12, 64)
     assert pkv.pkv_decode_workspace_size(4, 8, 3, 128, 16) == 0      # heads not divisible
     assert pkv.pkv_decode_workspace_size(4, 8, 2, 96, 16) == 0       # unsupported head_dim
     assert pkv.pkv_decode_workspace_size(0, 8, 2, 64, 0) == 0

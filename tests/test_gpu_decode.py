@@ -69,7 +69,8 @@ def test_split_count_sweep(variant, workers):
 @pytest.mark.parametrize("mode", ["auto", "persistent"])
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (8, 2, 64), (14, 2, 64), (32, 8, 128),
-                                      (16, 1, 128), (24, 2, 64), (4, 4, 64)])
+                                      (16, 1, 128), (24, 2, 64), (4, 4, 64), (40, 2, 128),
+                                      (32, 1, 64), (9, 1, 128)])
 def test_group_sizes_and_edge_lengths(variant, hq, hkv, d, mode):
     # "auto": these small batches take the one-item-per-cluster launch;
     # "persistent": the same batch through the persistent workers + reduce
