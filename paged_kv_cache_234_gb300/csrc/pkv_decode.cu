@@ -9,9 +9,9 @@
 //   out[s][h] = sum_t softmax_t(scale * <q[s][h], K_t>) V_t,  t < ctx[s],
 // with query head h reading kv head h / (Hq / Hkv).
 //
-// Work decomposition.  A work item is (sequence, kv head, group of up to 8
-// query heads of that kv head); its pages are the sequence's 16-token
-// blocks.  All items' pages form one stream of T pages, and every warp of a
+// Work decomposition.  A work item is (sequence, kv head, up to 8 query heads
+// of that kv head, or up to 16 as two groups of 8 when the kv head has more
+// than 8); its pages are the sequence's 16-token blocks.  All items' pages form one stream of T pages, and every warp of a
 // persistent grid (one worker per resident warp -- about seven per SM for
 // fp16 at head_dim 128 -- and at most four per item)
 // streams one contiguous, equal share of it, so every SM moves the same
@@ -29,10 +29,12 @@
 // the stage's mbarrier; the ring keeps the next stages in flight while the
 // warp computes on the oldest one.
 //
-// Per page, the GQA group's query heads (up to 8) share one read of K and V:
+// Per page, the item's query heads share one read of K and V, per group of 8:
 //   S^T[16 tok][8 heads] = K_page[16 x d] . Q^T      (m16n8k16, f16 -> f32)
 //   online softmax in base 2, one update per stage
 //   O^T[d][8 heads]     += V_page^T[d x 16] . P^T    (m16n8k16, f16 -> f32)
+// (with two groups, each K and V fragment is loaded and widened once and
+// enters both groups' mma).
 // FP8 (OCP E4M3) codes are widened to f16 exactly by cvt.rn.f16x2.e4m3x2; the
 // K and V scales apply as for INT8.
 // INT8 codes are widened to f16 exactly by byte permutes: a code c placed
@@ -64,7 +66,7 @@ namespace {
 constexpr int kWarps = 4;  // workers per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kPage = 16;              // tokens per block
-constexpr int kItemHeads = 8;          // query heads per work item (mma N)
+constexpr int kItemHeads = 8;          // query heads per group (mma N); an item has 1 or 2
 constexpr int kMaxWorkers = 4096;      // workspace is sized for at most this many
 constexpr int kMaxWorkersPerItem = 4;  // measured on GB300: 8 x 512, 32 x 1024 and Qwen2-
                                        // shape batches run 10-30 % faster than with one
