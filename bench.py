@@ -306,8 +306,9 @@ def run_profile(args):
     if args.profile == "int8-small":
         w = W.make("c2_8x512")
     else:
-        w = W.build(CONFIG + "_pool16k", num_heads=32, num_kv_heads=8, head_dim=128,
-                    num_blocks=16384, context_lens=[2048] * 64, seed=1005)
+        w = W.build(CONFIG + "_pool16k", num_heads=128 if args.profile == "int8-g16" else 32,
+                    num_kv_heads=8, head_dim=128, num_blocks=16384, context_lens=[2048] * 64,
+                    seed=1005)
     n, hq, d = w.query.shape
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     kf, vf = dev(w.k_pool), dev(w.v_pool)
@@ -321,7 +322,7 @@ def run_profile(args):
         vs = torch.zeros_like(ks)
         tails = dev(w.tail_block_ids())
         call = lambda: pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, tails)
-    elif args.profile in ("int8", "fp8", "int8-small"):
+    elif args.profile in ("int8", "fp8", "int8-small", "int8-g16"):
         kc = torch.zeros(w.k_pool.shape, dtype=torch.int8, device="cuda")
         vc = torch.zeros_like(kc)
         ks = torch.zeros(w.k_pool.shape[:2], dtype=torch.float32, device="cuda")
@@ -582,11 +583,12 @@ def main():
                     help="with --report-configs: comma-separated configuration names to "
                          "report (default: all)")
     ap.add_argument("--profile", choices=["int8", "fp8", "fp16", "quantize", "append", "evict",
-                                          "int8-small"],
+                                          "int8-small", "int8-g16"],
                     help="profiling run: the same batch over a 16384-block pool (eviction: "
                          "a 65536-block pool; int8-small: the 8 x 512 batch, whose INT8 "
-                         "decode takes the one-item-per-cluster launch), only warm-up + "
-                         "timed calls of one kernel, no report line")
+                         "decode takes the one-item-per-cluster launch; int8-g16: the same "
+                         "KV with 128 query heads, 16 per kv head), only warm-up + timed "
+                         "calls of one kernel, no report line")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
