@@ -80,3 +80,37 @@ def test_scale_spread_over_forced_splits(variant, workers):
     ref, _ = oracle_decode(w, variant, codes)
     assert st == 0
     assert_close(got, ref, f"workers={workers}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("mag", ["hot-block-x100-v2^-8", "q-sd10-k2^-4-v2^-12", "v2^4"])
+@pytest.mark.parametrize("hq,hkv", [(32, 2), (64, 1)])
+def test_magnitudes_two_groups_per_item(variant, mag, hq, hkv):
+    # 16 and 64 query heads per kv head: work items of two groups of 8 share
+    # every page, and the V-scale reference rescales both groups' accumulators
+    w = W.random_case(360 + list(MAGNITUDES).index(mag) + hq, num_seqs=4, num_heads=hq,
+                      num_kv_heads=hkv, head_dim=128, context_lens=[1, 300, 777, 2000],
+                      **MAGNITUDES[mag])
+    codes = None if variant == "fp16" else oracle_codes(w, variant == "fp8")
+    got, st = gpu_decode(w, variant, codes)
+    ref, flags = oracle_decode(w, variant, codes)
+    assert st == 0 and not flags.any()
+    assert_close(got, ref, f"g{hq // hkv}/{mag}/{variant}")
+
+
+@pytest.mark.parametrize("variant", ["int8", "fp8"])
+@pytest.mark.parametrize("workers", [1, 7, 64])
+def test_two_groups_scale_spread_over_forced_splits(variant, workers):
+    # records of 16 heads merged by the reduce, V scales 100x apart
+    w = W.random_case(370, num_seqs=3, num_heads=32, num_kv_heads=2, head_dim=128,
+                      context_lens=[2000, 333, 48], v_hot_mult=100.0, v_mult=2.0 ** -8)
+    codes = oracle_codes(w, variant == "fp8")
+    ensure_built()
+    try:
+        pkv.pkv_set_decode_workers(workers)
+        got, st = gpu_decode(w, variant, codes)
+    finally:
+        pkv.pkv_set_decode_workers(0)
+    ref, _ = oracle_decode(w, variant, codes)
+    assert st == 0
+    assert_close(got, ref, f"two groups, workers={workers}")
