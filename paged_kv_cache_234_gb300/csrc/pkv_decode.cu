@@ -73,6 +73,9 @@ constexpr int kMaxWorkersPerItem = 4;  // measured on GB300: 8 x 512, 32 x 1024 
                                        // worker per resident warp
 constexpr int kMaxSeqs = 8192;         // per-sequence tables live in shared memory
 constexpr int kMaxCluster = 8;         // CTAs per cluster in the one-item-per-cluster mode
+constexpr int kMaxClusterStages = 2;   // the cluster mode only while a warp has at most this
+                                       // many stages of its item at the largest cluster
+constexpr int kMinPagesPerWorker = 8;  // persistent workers: at least this many pages each
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
 constexpr float kPScale = 32768.f;     // probabilities enter PV as 2^15 p (see the main loop)
 constexpr float kPScaleInv = 1.f / 32768.f;
@@ -1412,6 +1415,131 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const DecodeArgs p)
     }
 }
 
+// Split-context reduce for items cut into many pieces (a few long contexts
+// spread over the whole grid).  One CTA of kManyWarps warps per (item, query
+// head) task: warp k merges pieces' chunks k, k + kManyWarps, ... of eight
+// (each chunk's loads all in flight, merged online into a running max, sum
+// and accumulator), then the warps' partials are combined in shared memory:
+//   out = sum_w 2^(M_w - M) acc_w / sum_w 2^(M_w - M) L_w,  M = max_w M_w
+// Used instead of reduce_kernel when the grid has more than eight workers
+// per item on average; the merge is the same, in a different order.
+constexpr int kManyWarps = 8;
+constexpr int kManyThreads = kManyWarps * 32;
+
+template <int kD>
+__global__ void __launch_bounds__(kManyThreads) reduce_many_kernel(const DecodeArgs p)
+{
+    constexpr int kC = kD / 32;  // accumulator floats per lane
+    extern __shared__ __align__(16) uint8_t msmem[];
+    int32_t *prefix = reinterpret_cast<int32_t *>(msmem);
+    int32_t *ctxs = prefix + p.num_seqs + 1;
+    __shared__ float sm_m[kManyWarps], sm_l[kManyWarps];
+    __shared__ int sm_bad[kManyWarps];
+    __shared__ __align__(16) float sm_acc[kManyWarps][kD];
+    build_page_tables<kManyThreads>(p, prefix, ctxs);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int W = p.num_workers;
+    const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
+    const int64_t per_seq = static_cast<int64_t>(p.items_per_seq) * p.rec_heads;
+    const int64_t ntasks = per_seq * p.num_seqs;
+    ptx::griddep_wait();  // the decode grid's records are complete and visible
+    for (int64_t t = blockIdx.x; t < ntasks; t += gridDim.x) {
+        const int seq = static_cast<int>(t / per_seq);
+        const int rem = static_cast<int>(t - seq * per_seq);
+        const int item = rem / p.rec_heads;
+        const int h = rem - item * p.rec_heads;
+        const int kvh = item / p.qgroups, qg = item - kvh * p.qgroups;
+        const int gh = min(p.item_heads, p.group - qg * p.item_heads);
+        const int npages = prefix[seq + 1] - prefix[seq];
+        if (h >= gh || npages == 0) continue;
+        const int64_t s0 = static_cast<int64_t>(p.items_per_seq) * prefix[seq] +
+                           static_cast<int64_t>(item) * npages;  // the item's first page
+        const int64_t last = s0 + npages - 1;
+        const int wf = static_cast<int>(worker_of(s0, total, W));
+        const int nw = static_cast<int>(worker_of(last, total, W)) - wf + 1;
+        if (nw == 1) continue;  // whole inside one worker: finished by the decode
+        const int slot0 = s0 == muldiv(wf, total, W) ? 0 : 1;
+        // the record of piece j of this item (null: a worker with no pages)
+        auto rec_of = [&](int j) -> const float * {
+            const int64_t w = wf + j;
+            if (j > 0 && muldiv(w, total, W) == muldiv(w + 1, total, W)) return nullptr;
+            const int slot = j == 0 ? slot0 : 0;
+            return p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
+        };
+        float M = -INFINITY, L = 0.f, acc[kC];
+#pragma unroll
+        for (int i = 0; i < kC; ++i) acc[i] = 0.f;
+        bool bad = false;
+        for (int c0 = warp * 8; c0 < nw; c0 += kManyWarps * 8) {
+            float m[8], l[8], v[8][kC];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float *r = c0 + u < nw ? rec_of(c0 + u) : nullptr;
+                if (r) {
+                    m[u] = __ldcg(r);
+                    l[u] = __ldcg(r + 1);
+#pragma unroll
+                    for (int i = 0; i < kC; ++i) v[u][i] = __ldcg(r + 4 + lane + 32 * i);
+                } else {
+                    m[u] = -INFINITY;
+                    l[u] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < kC; ++i) v[u][i] = 0.f;
+                }
+            }
+            float Mn = M;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) Mn = fmaxf(Mn, m[u]);
+            const float fo = M == -INFINITY ? 0.f : ptx::ex2(M - Mn);
+            L *= fo;
+#pragma unroll
+            for (int i = 0; i < kC; ++i) acc[i] *= fo;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float f = m[u] == -INFINITY ? 0.f : ptx::ex2(m[u] - Mn);
+                bad |= l[u] < 0.f;
+                L += f * l[u];
+#pragma unroll
+                for (int i = 0; i < kC; ++i) acc[i] += f * v[u][i];
+            }
+            M = Mn;
+        }
+        if (lane == 0) {
+            sm_m[warp] = M;
+            sm_l[warp] = L;
+            sm_bad[warp] = bad ? 1 : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < kC; ++i) sm_acc[warp][lane + 32 * i] = acc[i];
+        __syncthreads();
+        if (warp == 0) {
+            float Mt = -INFINITY;
+            bool anybad = false;
+#pragma unroll
+            for (int k = 0; k < kManyWarps; ++k) {
+                Mt = fmaxf(Mt, sm_m[k]);
+                anybad |= sm_bad[k] != 0;
+            }
+            float Lt = 0.f, out[kC];
+#pragma unroll
+            for (int i = 0; i < kC; ++i) out[i] = 0.f;
+#pragma unroll
+            for (int k = 0; k < kManyWarps; ++k) {
+                const float f = sm_m[k] == -INFINITY ? 0.f : ptx::ex2(sm_m[k] - Mt);
+                Lt += f * sm_l[k];
+#pragma unroll
+                for (int i = 0; i < kC; ++i) out[i] += f * sm_acc[k][lane + 32 * i];
+            }
+            const int h0 = kvh * p.group + qg * p.item_heads;
+            float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
+            const float inv = anybad ? 0.f : 1.f / Lt;
+#pragma unroll
+            for (int i = 0; i < kC; ++i) dst[lane + 32 * i] = anybad ? 0.f : out[i] * inv;
+        }
+        __syncthreads();  // the shared partials are free for the next task
+    }
+}
+
 // Launch with programmatic stream serialisation: the kernel may begin while
 // the previous kernel on the stream drains; it calls griddepcontrol.wait
 // before touching that kernel's results.
@@ -1587,11 +1715,15 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
         const int64_t stage_pages = static_cast<int64_t>(kWarps) * C::kPPS;
         const int64_t pages = (sh.ctx_cap + kPage - 1) / kPage;
         int64_t cl = (pages + stage_pages - 1) / stage_pages;
+        // long items stream faster over the persistent workers, whose number
+        // follows the pages rather than the items
+        const bool cluster_ok = cl <= static_cast<int64_t>(kMaxClusterStages) * kMaxCluster;
         if (cl > kMaxCluster) cl = kMaxCluster;
         if (items > 0 && cl > resident / items) cl = resident / items;
         // the records pushed to a CTA take shared memory, so a smaller
         // cluster may be what fits in one wave: halve until it does
-        for (; cap == 0 && cl >= 1 && items * cl <= resident; cl = cl > 1 ? cl / 2 : 0) {
+        for (; cap == 0 && cluster_ok && cl >= 1 && items * cl <= resident;
+             cl = cl > 1 ? cl / 2 : 0) {
             const int hpc = static_cast<int>((sh.rec_heads + cl - 1) / cl);
             const size_t smem_cl = 1024 + C::crec_offset(call.num_seqs) +
                                    C::crec_bytes(static_cast<int>(cl) * kWarps, hpc);
@@ -1622,12 +1754,15 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     if (workers > kMaxWorkers) workers = kMaxWorkers;
     if (cap > 0 && workers > cap) workers = cap;
     if (workers > sh.max_pages) workers = sh.max_pages;
-    // at most kMaxWorkersPerItem workers per item: small batches then split
-    // each item into a few pieces (the reduce's fast path) rather than
-    // spreading it one page per warp
+    // at most kMaxWorkersPerItem workers per item, or one per
+    // kMinPagesPerWorker pages if that is more: short items then split into a
+    // few pieces (the reduce's fast path) rather than one page per warp, and
+    // long items still spread over the whole grid
     const int64_t by_items =
         static_cast<int64_t>(kMaxWorkersPerItem) * call.num_seqs * sh.items_per_seq;
-    if (workers > by_items) workers = by_items;
+    const int64_t by_pages = sh.max_pages / kMinPagesPerWorker;
+    const int64_t limit = by_items > by_pages ? by_items : by_pages;
+    if (workers > limit) workers = limit;
     if (workers < 1) workers = 1;
 
     CUtensorMap tmk, tmv;
@@ -1677,42 +1812,46 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
         return PKV_ERR_CUDA;
     }
     if (workers > 1) {
-        constexpr int kRedWarps = kRedThreads / 32;
-        const int64_t tasks =
-            static_cast<int64_t>(call.num_seqs) * sh.items_per_seq * sh.rec_heads;
-        int64_t rgrid = (tasks + kRedWarps - 1) / kRedWarps;
+        const int64_t items = static_cast<int64_t>(call.num_seqs) * sh.items_per_seq;
+        const int64_t tasks = items * sh.rec_heads;
+        // items cut into more than eight pieces on average: a CTA per task
+        // (its warps share the pieces); else a warp per task
+        const int many = workers > 8 * items ? 1 : 0;
+        const int rthreads = many ? kManyThreads : kRedThreads;
+        const int64_t per_cta = many ? 1 : kRedThreads / 32;
+        int64_t rgrid = (tasks + per_cta - 1) / per_cta;
         const size_t rsmem = static_cast<size_t>(2 * call.num_seqs + 1) * sizeof(int32_t);
-        auto rk = reduce_kernel<kD>;
+        auto rk = many ? reduce_many_kernel<kD> : reduce_kernel<kD>;
         int red_per_sm = 0;
         {
-            // the per-sequence tables of the largest batch, once per device;
-            // a grid of at most one wave (warps then loop over the tasks)
-            static int red_ready[64] = {};
-            static size_t red_smem[64] = {};
-            static int red_occ[64] = {};
+            // the per-sequence tables of the largest batch, once per device
+            // and kernel; a grid of at most one wave (tasks then loop)
+            static int red_ready[64][2] = {};
+            static size_t red_smem[64][2] = {};
+            static int red_occ[64][2] = {};
             std::lock_guard<std::mutex> lock(g_cfg_mu);
             const int dv = di.device & 63;
-            if (!red_ready[dv]) {
+            if (!red_ready[dv][many]) {
                 if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>((2 * kMaxSeqs + 1) * sizeof(int32_t))) !=
                     cudaSuccess)
                     return PKV_ERR_CUDA;
-                red_ready[dv] = 1;
-                red_smem[dv] = ~size_t(0);
+                red_ready[dv][many] = 1;
+                red_smem[dv][many] = ~size_t(0);
             }
-            if (red_smem[dv] != rsmem) {
+            if (red_smem[dv][many] != rsmem) {
                 int v = 0;
-                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, rk, kRedThreads, rsmem) !=
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, rk, rthreads, rsmem) !=
                     cudaSuccess)
                     return PKV_ERR_CUDA;
-                red_smem[dv] = rsmem;
-                red_occ[dv] = v;
+                red_smem[dv][many] = rsmem;
+                red_occ[dv][many] = v;
             }
-            red_per_sm = red_occ[dv];
+            red_per_sm = red_occ[dv][many];
         }
         const int64_t wave = static_cast<int64_t>(red_per_sm > 0 ? red_per_sm : 1) * di.num_sms;
         if (rgrid > wave) rgrid = wave;
-        if (launch_pdl(rk, static_cast<unsigned>(rgrid), kRedThreads, rsmem, st, 0, args) !=
+        if (launch_pdl(rk, static_cast<unsigned>(rgrid), rthreads, rsmem, st, 0, args) !=
             cudaSuccess) {
             cudaGetLastError();
             return PKV_ERR_CUDA;
