@@ -3,6 +3,10 @@
 * One long sequence among short ones: its single work item is spread over
   dozens of workers, so the split-context reduce merges more than 32 pieces
   of one item (the path that reads the pieces' maxima 32 at a time).
+* A few long items over the whole grid (one worker per eight pages): more
+  than eight pieces per item on average, merged by the CTA-per-task reduce
+  whose warps each take chunks of eight pieces; with a maximum context far
+  above the real ones, most workers hold no pages at all.
 * The largest batch the decode accepts (8192 sequences): the per-sequence
   tables fill the most shared memory and are built in many passes.
 * A quantize + decode step captured once in a CUDA graph and replayed on new
@@ -42,6 +46,32 @@ def test_one_long_item_over_many_workers(variant, workers):
     ref, flags = oracle_decode(w, variant, codes)
     assert st == 0 and not flags.any()
     assert_close(got, ref, f"long item, workers={workers}")
+
+
+MANY_PIECES = [
+    # (query heads, kv heads, head_dim, context lengths, maximum context)
+    (32, 8, 128, [32768], None),         # 8 items of 2048 pages, ~256 pieces each
+    (16, 1, 64, [16384, 3, 0], None),    # two groups of 8 query heads per item
+    (8, 1, 128, [2048, 0, 0, 0], 16384),  # most workers empty: the bound is 8x the pages
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("case", range(len(MANY_PIECES)))
+def test_items_over_many_pieces(variant, case):
+    hq, hkv, d, lens, mcl = MANY_PIECES[case]
+    w = W.random_case(95 + case, num_seqs=len(lens), num_heads=hq, num_kv_heads=hkv,
+                      head_dim=d, context_lens=lens)
+    codes = oracle_codes(w, variant == "fp8")
+    tables = w.block_tables
+    if mcl is not None:  # table rows wide enough for the maximum (block 0 past the ends)
+        tables = np.zeros((len(lens), mcl // 16), dtype=np.int32)
+        tables[:, :w.block_tables.shape[1]] = w.block_tables
+    got, st = gpu_decode(w, variant, codes, max_context_len=mcl, tables=tables)
+    ref, flags = oracle_decode(w, variant, codes, max_context_len=mcl, tables=tables)
+    assert st == 0 and not flags.any()
+    assert_close(got, ref, f"many pieces, case {case}")
+    assert np.all(got[w.context_lens == 0] == 0)
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
