@@ -305,6 +305,12 @@ def run_profile(args):
     pkv_build.build()
     if args.profile == "int8-small":
         w = W.make("c2_8x512")
+    elif args.profile == "int8-d64":
+        w = W.build("qwen2_512x2048", num_heads=14, num_kv_heads=2, head_dim=64,
+                    num_blocks=65536 + 64, context_lens=[2048] * 512, seed=1007)
+    elif args.profile == "int8-long":
+        w = W.build("long_1x131072", num_heads=32, num_kv_heads=8, head_dim=128,
+                    num_blocks=8192 + 64, context_lens=[131072], seed=1006)
     else:
         w = W.build(CONFIG + "_pool16k", num_heads=128 if args.profile == "int8-g16" else 32,
                     num_kv_heads=8, head_dim=128, num_blocks=16384, context_lens=[2048] * 64,
@@ -322,7 +328,7 @@ def run_profile(args):
         vs = torch.zeros_like(ks)
         tails = dev(w.tail_block_ids())
         call = lambda: pkv.pkv_quantize_blocks(kf, vf, kc, vc, ks, vs, tails)
-    elif args.profile in ("int8", "fp8", "int8-small", "int8-g16"):
+    elif args.profile in ("int8", "fp8", "int8-small", "int8-g16", "int8-long", "int8-d64"):
         kc = torch.zeros(w.k_pool.shape, dtype=torch.int8, device="cuda")
         vc = torch.zeros_like(kc)
         ks = torch.zeros(w.k_pool.shape[:2], dtype=torch.float32, device="cuda")
@@ -583,11 +589,14 @@ def main():
                     help="with --report-configs: comma-separated configuration names to "
                          "report (default: all)")
     ap.add_argument("--profile", choices=["int8", "fp8", "fp16", "quantize", "append", "evict",
-                                          "int8-small", "int8-g16"],
+                                          "int8-small", "int8-g16", "int8-long", "int8-d64"],
                     help="profiling run: the same batch over a 16384-block pool (eviction: "
                          "a 65536-block pool; int8-small: the 8 x 512 batch, whose INT8 "
                          "decode takes the one-item-per-cluster launch; int8-g16: the same "
-                         "KV with 128 query heads, 16 per kv head), only warm-up + timed "
+                         "KV with 128 query heads, 16 per kv head; int8-long: one sequence "
+                         "of 131072 tokens, the same KV bytes; int8-d64: 512 x 2048 in the "
+                         "Qwen2-0.5B attention shape, 14 query / 2 kv heads of 64, the same "
+                         "KV bytes), only warm-up + timed "
                          "calls of one kernel, no report line")
     args = ap.parse_args()
     ws, rank, local = dist_setup()

@@ -90,7 +90,7 @@ struct DecodeArgs {
     const int32_t *context_lens;
     const float *k_scales;
     const float *v_scales;
-    float *partials;     // [num_workers * 2][rec_heads][head_dim + 4]
+    float *partials;     // [num_workers * 2][rec_heads][head_dim + 4]: m, l, 0, -, acc
     int32_t *dev_status;
     int num_seqs, num_heads, num_kv_heads;
     int group;           // query heads per kv head
@@ -1149,13 +1149,17 @@ __global__ void __launch_bounds__(kThreads, kG == 1 ? Cfg<kKv, kD>::kMinCtas : (
                     }
                     fA = fB = (kInt8 ? vref : 1.f) * kPScaleInv;  // accumulators in V units
                     if (g == 0) {
+                        // m, l, and a zero word (the many-piece reduce counts
+                        // its CTAs in the first piece's)
                         if (hA < gh) {
                             dstA[-4] = m0[gi];
                             dstA[-3] = piece_bad ? -1.f : l0[gi];
+                            if constexpr (!kClust) dstA[-2] = 0.f;
                         }
                         if (hB < gh) {
                             dstB[-4] = m1[gi];
                             dstB[-3] = piece_bad ? -1.f : l1[gi];
+                            if constexpr (!kClust) dstB[-2] = 0.f;
                         }
                     }
                 }
@@ -1416,18 +1420,25 @@ __global__ void __launch_bounds__(kRedThreads) reduce_kernel(const DecodeArgs p)
 }
 
 // Split-context reduce for items cut into many pieces (a few long contexts
-// spread over the whole grid).  One CTA of kManyWarps warps per (item, query
-// head) task: warp k merges pieces' chunks k, k + kManyWarps, ... of eight
-// (each chunk's loads all in flight, merged online into a running max, sum
-// and accumulator), then the warps' partials are combined in shared memory:
-//   out = sum_w 2^(M_w - M) acc_w / sum_w 2^(M_w - M) L_w,  M = max_w M_w
-// Used instead of reduce_kernel when the grid has more than eight workers
-// per item on average; the merge is the same, in a different order.
+// spread over the whole grid).  S CTAs (1-8) of kManyWarps warps share each
+// (item, query head) task: warp k of CTA r merges the chunks of eight pieces
+// numbered r * kManyWarps + k, then that plus A * kManyWarps, ... (A: the
+// task's active CTAs, those with pieces; each chunk's loads all in flight,
+// merged online into a running max, sum and accumulator), and the CTA
+// combines its warps' partials in shared memory.  With one active CTA that
+// is the output.  Otherwise CTA r stores its partial in the record of piece
+// 64 r (read by this CTA alone, already consumed), and counts itself in the
+// zero word of piece 0's record; the CTA that arrives last combines the A
+// partials in rank order, so the bits do not depend on the arrival order:
+//   out = sum_r 2^(M_r - M) acc_r / sum_r 2^(M_r - M) L_r,  M = max_r M_r
+// No CTA waits for another.  Used instead of reduce_kernel when the grid has
+// more than eight workers per item on average.
 constexpr int kManyWarps = 8;
 constexpr int kManyThreads = kManyWarps * 32;
+constexpr int kManyChunk = kManyWarps * 8;  // pieces one CTA takes per round
 
 template <int kD>
-__global__ void __launch_bounds__(kManyThreads) reduce_many_kernel(const DecodeArgs p)
+__global__ void __launch_bounds__(kManyThreads) reduce_many_kernel(const DecodeArgs p, int S)
 {
     constexpr int kC = kD / 32;  // accumulator floats per lane
     extern __shared__ __align__(16) uint8_t msmem[];
@@ -1438,12 +1449,14 @@ __global__ void __launch_bounds__(kManyThreads) reduce_many_kernel(const DecodeA
     __shared__ __align__(16) float sm_acc[kManyWarps][kD];
     build_page_tables<kManyThreads>(p, prefix, ctxs);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = static_cast<int>(blockIdx.x % S);
     const int W = p.num_workers;
     const int64_t total = static_cast<int64_t>(p.items_per_seq) * prefix[p.num_seqs];
     const int64_t per_seq = static_cast<int64_t>(p.items_per_seq) * p.rec_heads;
     const int64_t ntasks = per_seq * p.num_seqs;
+    const int64_t ngroups = gridDim.x / S;
     ptx::griddep_wait();  // the decode grid's records are complete and visible
-    for (int64_t t = blockIdx.x; t < ntasks; t += gridDim.x) {
+    for (int64_t t = blockIdx.x / S; t < ntasks; t += ngroups) {
         const int seq = static_cast<int>(t / per_seq);
         const int rem = static_cast<int>(t - seq * per_seq);
         const int item = rem / p.rec_heads;
@@ -1458,28 +1471,36 @@ __global__ void __launch_bounds__(kManyThreads) reduce_many_kernel(const DecodeA
         const int wf = static_cast<int>(worker_of(s0, total, W));
         const int nw = static_cast<int>(worker_of(last, total, W)) - wf + 1;
         if (nw == 1) continue;  // whole inside one worker: finished by the decode
+        const int active = min(S, (nw + kManyChunk - 1) / kManyChunk);
+        if (r >= active) continue;
         const int slot0 = s0 == muldiv(wf, total, W) ? 0 : 1;
-        // the record of piece j of this item (null: a worker with no pages)
+        // the record slot of piece j of this item (that of a worker with no
+        // pages is never written by the decode)
+        auto rec_at = [&](int j) -> float * {
+            const int64_t w = wf + j;
+            const int slot = j == 0 ? slot0 : 0;
+            return p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
+        };
+        // the record of piece j (null: a worker with no pages)
         auto rec_of = [&](int j) -> const float * {
             const int64_t w = wf + j;
             if (j > 0 && muldiv(w, total, W) == muldiv(w + 1, total, W)) return nullptr;
-            const int slot = j == 0 ? slot0 : 0;
-            return p.partials + ((w * 2 + slot) * p.rec_heads + h) * (kD + 4);
+            return rec_at(j);
         };
         float M = -INFINITY, L = 0.f, acc[kC];
 #pragma unroll
         for (int i = 0; i < kC; ++i) acc[i] = 0.f;
         bool bad = false;
-        for (int c0 = warp * 8; c0 < nw; c0 += kManyWarps * 8) {
+        for (int c0 = (r * kManyWarps + warp) * 8; c0 < nw; c0 += active * kManyChunk) {
             float m[8], l[8], v[8][kC];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const float *r = c0 + u < nw ? rec_of(c0 + u) : nullptr;
-                if (r) {
-                    m[u] = __ldcg(r);
-                    l[u] = __ldcg(r + 1);
+                const float *rp = c0 + u < nw ? rec_of(c0 + u) : nullptr;
+                if (rp) {
+                    m[u] = __ldcg(rp);
+                    l[u] = __ldcg(rp + 1);
 #pragma unroll
-                    for (int i = 0; i < kC; ++i) v[u][i] = __ldcg(r + 4 + lane + 32 * i);
+                    for (int i = 0; i < kC; ++i) v[u][i] = __ldcg(rp + 4 + lane + 32 * i);
                 } else {
                     m[u] = -INFINITY;
                     l[u] = 0.f;
@@ -1513,6 +1534,7 @@ __global__ void __launch_bounds__(kManyThreads) reduce_many_kernel(const DecodeA
         for (int i = 0; i < kC; ++i) sm_acc[warp][lane + 32 * i] = acc[i];
         __syncthreads();
         if (warp == 0) {
+            // this CTA's warps, in warp order (L < 0: a bad piece)
             float Mt = -INFINITY;
             bool anybad = false;
 #pragma unroll
@@ -1520,21 +1542,75 @@ __global__ void __launch_bounds__(kManyThreads) reduce_many_kernel(const DecodeA
                 Mt = fmaxf(Mt, sm_m[k]);
                 anybad |= sm_bad[k] != 0;
             }
-            float Lt = 0.f, out[kC];
+            float Lt = 0.f, o[kC];
 #pragma unroll
-            for (int i = 0; i < kC; ++i) out[i] = 0.f;
+            for (int i = 0; i < kC; ++i) o[i] = 0.f;
 #pragma unroll
             for (int k = 0; k < kManyWarps; ++k) {
                 const float f = sm_m[k] == -INFINITY ? 0.f : ptx::ex2(sm_m[k] - Mt);
                 Lt += f * sm_l[k];
 #pragma unroll
-                for (int i = 0; i < kC; ++i) out[i] += f * sm_acc[k][lane + 32 * i];
+                for (int i = 0; i < kC; ++i) o[i] += f * sm_acc[k][lane + 32 * i];
             }
-            const int h0 = kvh * p.group + qg * p.item_heads;
-            float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
-            const float inv = anybad ? 0.f : 1.f / Lt;
+            bool write = true;
+            if (active > 1) {
+                float *part = rec_at(r * kManyChunk);
+                if (lane == 0) {
+                    part[0] = Mt;
+                    part[1] = anybad ? -1.f : Lt;
+                }
 #pragma unroll
-            for (int i = 0; i < kC; ++i) dst[lane + 32 * i] = anybad ? 0.f : out[i] * inv;
+                for (int i = 0; i < kC; ++i) part[4 + lane + 32 * i] = o[i];
+                __threadfence();  // the partial is visible before the count
+                __syncwarp();
+                int prior = 0;
+                if (lane == 0)
+                    prior = atomicAdd(reinterpret_cast<int *>(rec_at(0) + 2), 1);
+                write = __shfl_sync(0xffffffffu, prior, 0) == active - 1;
+                if (write) {
+                    __threadfence();  // every other CTA's partial is visible
+                    // all partials' loads in flight at once, then the merge
+                    float mq[8], lq[8], vq[8][kC];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        mq[q] = -INFINITY;
+                        lq[q] = 0.f;
+#pragma unroll
+                        for (int i = 0; i < kC; ++i) vq[q][i] = 0.f;
+                        if (q < active) {
+                            const float *pq = rec_at(q * kManyChunk);
+                            mq[q] = __ldcg(pq);
+                            lq[q] = __ldcg(pq + 1);
+#pragma unroll
+                            for (int i = 0; i < kC; ++i) vq[q][i] = __ldcg(pq + 4 + lane + 32 * i);
+                        }
+                    }
+                    Mt = -INFINITY;
+                    anybad = false;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        Mt = fmaxf(Mt, mq[q]);
+                        anybad |= lq[q] < 0.f;
+                    }
+                    Lt = 0.f;
+#pragma unroll
+                    for (int i = 0; i < kC; ++i) o[i] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float f = mq[q] == -INFINITY ? 0.f : ptx::ex2(mq[q] - Mt);
+                        Lt += f * lq[q];
+#pragma unroll
+                        for (int i = 0; i < kC; ++i) o[i] += f * vq[q][i];
+                    }
+                }
+            }
+            if (write) {
+                const int h0 = kvh * p.group + qg * p.item_heads;
+                float *dst = p.out + (static_cast<int64_t>(seq) * p.num_heads + h0 + h) * kD;
+                const float inv = anybad ? 0.f : 1.f / Lt;
+#pragma unroll
+                for (int i = 0; i < kC; ++i) dst[lane + 32 * i] = anybad ? 0.f : o[i] * inv;
+            }
         }
         __syncthreads();  // the shared partials are free for the next task
     }
@@ -1814,14 +1890,14 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
     if (workers > 1) {
         const int64_t items = static_cast<int64_t>(call.num_seqs) * sh.items_per_seq;
         const int64_t tasks = items * sh.rec_heads;
-        // items cut into more than eight pieces on average: a CTA per task
-        // (its warps share the pieces); else a warp per task
+        // items cut into more than eight pieces on average: CTAs per task
+        // (their warps share the pieces); else a warp per task
         const int many = workers > 8 * items ? 1 : 0;
         const int rthreads = many ? kManyThreads : kRedThreads;
-        const int64_t per_cta = many ? 1 : kRedThreads / 32;
-        int64_t rgrid = (tasks + per_cta - 1) / per_cta;
+        int64_t rgrid = (tasks + kRedThreads / 32 - 1) / (kRedThreads / 32);
         const size_t rsmem = static_cast<size_t>(2 * call.num_seqs + 1) * sizeof(int32_t);
-        auto rk = many ? reduce_many_kernel<kD> : reduce_kernel<kD>;
+        const void *rk = many ? reinterpret_cast<const void *>(reduce_many_kernel<kD>)
+                              : reinterpret_cast<const void *>(reduce_kernel<kD>);
         int red_per_sm = 0;
         {
             // the per-sequence tables of the largest batch, once per device
@@ -1850,9 +1926,22 @@ pkv_status launch(const DecodeCall &call, const Shape &sh)
             red_per_sm = red_occ[dv][many];
         }
         const int64_t wave = static_cast<int64_t>(red_per_sm > 0 ? red_per_sm : 1) * di.num_sms;
-        if (rgrid > wave) rgrid = wave;
-        if (launch_pdl(rk, static_cast<unsigned>(rgrid), rthreads, rsmem, st, 0, args) !=
-            cudaSuccess) {
+        cudaError_t le;
+        if (many) {
+            // up to 8 CTAs per task, as many as one wave allows
+            int split = 8;
+            while (split > 1 && tasks * split > wave) split /= 2;
+            int64_t groups = wave / split;
+            if (groups > tasks) groups = tasks;
+            if (groups < 1) groups = 1;
+            le = launch_pdl(reduce_many_kernel<kD>, static_cast<unsigned>(groups * split),
+                            kManyThreads, rsmem, st, 0, args, split);
+        } else {
+            if (rgrid > wave) rgrid = wave;
+            le = launch_pdl(reduce_kernel<kD>, static_cast<unsigned>(rgrid), kRedThreads, rsmem, st,
+                            0, args);
+        }
+        if (le != cudaSuccess) {
             cudaGetLastError();
             return PKV_ERR_CUDA;
         }

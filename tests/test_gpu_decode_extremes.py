@@ -4,9 +4,12 @@
   dozens of workers, so the split-context reduce merges more than 32 pieces
   of one item (the path that reads the pieces' maxima 32 at a time).
 * A few long items over the whole grid (one worker per eight pages): more
-  than eight pieces per item on average, merged by the CTA-per-task reduce
-  whose warps each take chunks of eight pieces; with a maximum context far
-  above the real ones, most workers hold no pages at all.
+  than eight pieces per item on average, merged by the reduce that gives
+  each task up to eight CTAs whose warps each take chunks of eight pieces
+  (the last CTA to finish combines the CTAs' partials in a fixed order, so
+  repeated calls give the same bits); with a maximum context far above the
+  real ones, most workers hold no pages at all, and with many tasks fewer
+  CTAs share a task and they loop over the tasks.
 * The largest batch the decode accepts (8192 sequences): the per-sequence
   tables fill the most shared memory and are built in many passes.
 * A quantize + decode step captured once in a CUDA graph and replayed on new
@@ -53,6 +56,8 @@ MANY_PIECES = [
     (32, 8, 128, [32768], None),         # 8 items of 2048 pages, ~256 pieces each
     (16, 1, 64, [16384, 3, 0], None),    # two groups of 8 query heads per item
     (8, 1, 128, [2048, 0, 0, 0], 16384),  # most workers empty: the bound is 8x the pages
+    (8, 1, 128, [300] * 16, 16384),     # 128 tasks: fewer CTAs per task
+    (8, 1, 64, [300] * 48, 16384),      # 384 tasks, more than one wave: CTAs loop
 ]
 
 
@@ -71,6 +76,9 @@ def test_items_over_many_pieces(variant, case):
     ref, flags = oracle_decode(w, variant, codes, max_context_len=mcl, tables=tables)
     assert st == 0 and not flags.any()
     assert_close(got, ref, f"many pieces, case {case}")
+    # the partials are combined in a fixed order, whichever CTA arrives last
+    again, st = gpu_decode(w, variant, codes, max_context_len=mcl, tables=tables)
+    assert st == 0 and np.array_equal(again.view(np.uint64), got.view(np.uint64))
     assert np.all(got[w.context_lens == 0] == 0)
 
 
