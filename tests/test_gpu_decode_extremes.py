@@ -83,6 +83,26 @@ def test_items_over_many_pieces(variant, case):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+def test_bad_block_ids_in_items_over_many_pieces(variant):
+    # ~190 pieces per long item, merged by several CTAs: a bad id in a middle
+    # piece (sequence 0) and in the first piece (sequence 2) zeroes exactly
+    # those sequences' outputs and sets the status flag
+    lens = [16384, 300, 16384]
+    w = W.random_case(98, num_seqs=3, num_heads=8, num_kv_heads=1, head_dim=128,
+                      context_lens=lens)
+    codes = oracle_codes(w, variant == "fp8")
+    tables = w.block_tables.copy()
+    tables[0, 700] = w.num_blocks + 5
+    tables[2, 3] = -5
+    got, st = gpu_decode(w, variant, codes, tables=tables)
+    ref, flags = oracle_decode(w, variant, codes, tables=tables)
+    assert st == pkv.PKV_DEV_BAD_BLOCK
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    assert np.all(ref[0] == 0) and np.all(ref[2] == 0)
+    assert_close(got, ref, "bad ids over many pieces")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 def test_largest_batch_of_sequences(variant):
     w = W.random_case(92, num_seqs=8192, num_heads=8, num_kv_heads=2, head_dim=64, max_ctx=40)
     codes = oracle_codes(w, variant == "fp8")
