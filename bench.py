@@ -980,10 +980,19 @@ def main():
     pipelined_copies(200)
     gc.disable()  # no collector pauses inside the host loops
     try:
+        if pg:
+            pg.barrier()
         e2e_pipe_ms = pipelined_in_place(Ke)
+        if pg:
+            pg.barrier()
         e2e_pipe_ce_ms = pipelined_copies(Ke)
     finally:
         gc.enable()
+    if pg:
+        # whole-job end-to-end: every rank's steps over the slowest rank's time
+        t = torch.tensor([e2e_pipe_ms, e2e_pipe_ce_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_pipe_ms, e2e_pipe_ce_ms = float(t[0].item()), float(t[1].item())
     assert all(torch.equal(x, hout) for x in hout2 + hout_ce2)
     # bytes of the step's host inputs (read in place; a query row is read by
     # each worker holding a piece of its item) and of its output
@@ -1068,19 +1077,20 @@ def main():
             "cow_copy_blocks_fp16": copies,
             "block_manager_host": bm_rate,
         },
-        "e2e": {"value": gbs(step_b, e2e_pipe_ce_ms), "unit": UNIT,
-                "h2d_bytes_per_step": total_b, "d2h_bytes_per_step": d2h, "steps": Ke,
+        "e2e": {"value": gbs(step_b * ws, e2e_pipe_ce_ms), "unit": UNIT,
+                "h2d_bytes_per_step": total_b * ws, "d2h_bytes_per_step": d2h * ws, "steps": Ke,
                 "form": "steps back to back through prepared calls; a copy stream copies each "
                         "step's staged inputs (query, block tables, context lengths, tail ids) "
                         "from pinned host memory into one of two device buffers while the step "
                         "before runs, and its output back into one of two pinned buffers, "
                         "which the host reads while the next step runs",
-                "in_place": {"value": gbs(step_b, e2e_pipe_ms),
+                "in_place": {"value": gbs(step_b * ws, e2e_pipe_ms),
                              "form": "labelled extra: steps back to back; the kernels read each "
                                      "step's staged inputs and write its output in place in "
                                      "pinned host memory (no copy operations)",
-                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                             "h2d_bytes_per_step": h2d * ws, "d2h_bytes_per_step": d2h * ws},
                 "per_step_sync": {
+                    "ranks": "rank 0 alone",
                     "form": "labelled extra: L2 flushed, then one step with a pair of events "
                             "around it and the host waiting for its output before the next",
                     "in_place": step_b * Ke / (e2e_ms * 1e-3) / 1e9,
