@@ -188,6 +188,13 @@ __device__ unsigned long long g_debug_stage_wait_ns = kWaitLimitNs;
 #ifndef PKV_F16_D128_WARPS_PER_SM
 #define PKV_F16_D128_WARPS_PER_SM 7
 #endif
+// fp16 d64: the same with 16 resident warps; measured on GB300 with 512 x 2048
+// in the Qwen2-0.5B shape (14 / 2 heads) and 128 x 2048 with 32 / 8 heads:
+// 92.0 and 87.3 us per call at 10 streaming warps per SM against 96.0 and
+// 91.2 us with all 16 (12: 94.7 / 90.1 us; 8: 99.8 / 91.9 us).
+#ifndef PKV_F16_D64_WARPS_PER_SM
+#define PKV_F16_D64_WARPS_PER_SM 10
+#endif
 
 template <int kPPS_, int kStages_, int kMinCtas_>
 struct Tune {
@@ -230,7 +237,8 @@ struct Cfg {
     static constexpr int kSwizzle = kRowBytes >= 128 ? 128 : 64;
     static constexpr int kStages = TuneOf<kKv, kD>::kStages;
     static constexpr int kMinCtas = TuneOf<kKv, kD>::kMinCtas;
-    static constexpr int kWarpsPerSm = kKv == kKvF16 && kD == 128 ? PKV_F16_D128_WARPS_PER_SM : 0;
+    static constexpr int kWarpsPerSm =
+        kKv != kKvF16 ? 0 : kD == 128 ? PKV_F16_D128_WARPS_PER_SM : PKV_F16_D64_WARPS_PER_SM;
     static_assert(kPPS == 1 || kPPS == 2, "one or two pages per stage");
     static constexpr int kHdrBytes = 32;  // per stage: bad[2], k scale[2], v scale[2]
     static constexpr int kStageRegion = kWarps * kStages * kStageBytes;
