@@ -11,16 +11,20 @@
 //
 // Work decomposition.  A work item is (sequence, kv head, up to 8 query heads
 // of that kv head, or up to 16 as two groups of 8 when the kv head has more
-// than 8); its pages are the sequence's 16-token blocks.  All items' pages form one stream of T pages, and every warp of a
-// persistent grid (one worker per resident warp -- about seven per SM for
-// fp16 at head_dim 128 -- and at most four per item)
+// than 8); its pages are the sequence's 16-token blocks.  All items' pages
+// form one stream of T pages, and every warp of a persistent grid (one worker
+// per resident warp -- seven per SM for fp16 at head_dim 128, ten at 64 --
+// and no more than the larger of four per item and one per eight pages)
 // streams one contiguous, equal share of it, so every SM moves the same
-// number of bytes whatever the mix of context lengths.  A worker's share is a run of "pieces": at most one
-// partial item at each end and whole items in between.  Whole items are
-// finished in place; a partial piece leaves (running max, running sum,
-// unnormalised accumulator) in the workspace, and the split-context reduce
-// kernel, launched as a programmatic dependent of the decode grid, merges the
-// pieces of every split item.
+// number of bytes whatever the mix of context lengths.  A worker's share is a
+// run of "pieces": at most one partial item at each end and whole items in
+// between.  Whole items are finished in place; a partial piece leaves
+// (running max, running sum, unnormalised accumulator) in the workspace, and
+// a split-context reduce kernel, launched as a programmatic dependent of the
+// decode grid, merges the pieces of every split item (a warp per item and
+// query head, or, for items cut into many pieces, several CTAs each).
+// Small batches run one item per thread-block cluster instead, merged in
+// distributed shared memory.
 //
 // Per worker (warp), pages flow through a private ring of S shared-memory
 // stages of one or two pages each.  Lane 0 issues TMA tile loads (16 rows x
