@@ -434,8 +434,11 @@ PKV_API size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv
  * Tuning and test control: cap the number of decode workers (one worker =
  * one warp streaming a contiguous range of KV pages; each range ends in a
  * partial result that the split-context reduce merges).  0 restores the
- * automatic choice (every resident warp of the device -- about seven per SM
- * for fp16 KV at head_dim 128 -- and at most four per item).  Process-wide.
+ * automatic choice: every resident warp of the device (seven per SM for fp16
+ * KV at head_dim 128, ten at 64), and no more than the larger of four per
+ * work item and one per eight pages of the longest possible page stream.  A
+ * cap also selects the persistent workers for batches that would otherwise
+ * run one item per thread-block cluster.  Process-wide.
  */
 PKV_API pkv_status pkv_set_decode_workers(int max_workers);
 

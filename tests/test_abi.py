@@ -40,6 +40,25 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_c_program_uses_the_abi(L):
+    # include/pkv.h compiled as C99 and libpkv.so linked by the system linker:
+    # the host-only calls of tests/c_abi/abi_smoke.c (no GPU needed)
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    exe = os.path.join(pkv_build.BUILD_DIR, "abi_smoke")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.dirname(HEADER), os.path.join(here, "c_abi", "abi_smoke.c"),
+                        "-L", pkv_build.BUILD_DIR, "-lpkv", "-Wl,-rpath," + pkv_build.BUILD_DIR,
+                        "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and "C ABI checks passed" in r.stdout, r.stdout + r.stderr
+
+
 def test_status_strings(L):
     for code in range(6):
         assert pkv.pkv_status_string(code)
